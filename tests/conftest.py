@@ -1,0 +1,21 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The built C-ABI library (built on demand; needs no GPU to load)."""
+    from kv_cache_token_bf16_gb300 import _build
+    _build.ensure_built()
+    from kv_cache_token_bf16_gb300 import binding
+    return binding.load()
