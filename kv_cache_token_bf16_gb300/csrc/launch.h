@@ -1,0 +1,21 @@
+// Host-side launchers of the eviction kernels (implemented in the .cu files).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "params.h"
+
+namespace evict {
+
+// Rows per compaction chunk for an element size of 2 (bf16) or 4 (fp32) bytes.
+int compact_chunk_rows(int dtype_bytes);
+
+cudaError_t launch_score(const GroupParams& P, int dtype_bytes, cudaStream_t st);
+cudaError_t launch_append(const GroupParams& P, int dtype_bytes, cudaStream_t st);
+// Raise the select kernel's dynamic shared memory limit to hold max_rows keys.
+cudaError_t prepare_select(int max_rows);
+cudaError_t launch_select(const GroupParams& P, cudaStream_t st);
+// Sets P.total_ctas.
+cudaError_t launch_compact(GroupParams& P, int dtype_bytes, cudaStream_t st);
+
+}  // namespace evict

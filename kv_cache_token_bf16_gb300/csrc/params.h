@@ -1,0 +1,55 @@
+// Launch parameters shared by the host orchestration and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace evict {
+
+// Up to this many layer caches can be updated by one set of launches.
+constexpr int kMaxGroup = 32;
+
+enum Method : int { kKNorm = 0, kQFilters = 1, kCurDKV = 2 };
+
+// Per-layer device pointers of one grouped update.
+struct LayerPtrs {
+  const void* k_in;        // [B, H, m, D] incoming keys
+  const void* v_in;        // [B, H, m, D] incoming values
+  const int32_t* pos_in;   // [B, m] or null (positions = offset + t)
+  void* kst;               // [B, H, cap, D] kept keys (in place)
+  void* vst;               // [B, H, cap, D] kept values
+  int32_t* pos_st;         // [B, H, cap]
+  float* score_st;         // [B, H, cap]
+  const float* filters;    // [H, D] (Q-Filters)
+  float* new_score;        // [B, H, new_stride] scores of incoming rows
+  int32_t* src_map;        // [B, H, cap] source row of each kept destination
+  int2* meta;              // [B, H] {first moved destination, old survivors}
+  int* flags;              // [B, H, flag_stride] read-done flags of compaction chunks
+};
+
+// Sizes common to every layer of a grouped update.
+struct Shape {
+  int batch, heads;        // B, H
+  int m;                   // incoming rows
+  int k;                   // kept rows before the call
+  int cap;                 // storage rows per (b, h)
+  int budget;
+  int n_sink, recent;
+  int new_stride;          // row stride of new_score (max_block)
+  int flag_stride;         // chunks per (b, h)
+  int n_layers;
+  int keep_low;            // KNorm keep-low: priority = -score
+  float sign;              // Q-Filters sign
+  int method;
+  long long offset;        // absolute position of the first incoming token
+};
+
+struct GroupParams {
+  Shape s;
+  int* ticket;             // compaction ticket counter (returns to 0 after each launch)
+  int* err;                // device error word
+  int total_ctas;          // compaction grid size
+  LayerPtrs L[kMaxGroup];
+};
+
+}  // namespace evict
