@@ -1,0 +1,601 @@
+"""Throughput of block KV-cache eviction on GB300 through libevict.
+
+Default workload: the Q-Filters calibrated Llama-3.2-3B-like layer stack —
+28 layers, 8 KV heads (24 query heads, GQA 3), D=128, bf16, B=1, one
+8192-token prefill block per layer, budget 1024, n_sink 4. One step = the
+whole hot path over that batch: every layer's cache is reset and absorbs
+the block (score, protected top-k, order-preserving compaction). Filters
+come from the GPU calibration (uncentered query SVD) run once before timing.
+
+Metric: cache tokens evicted-and-compacted per second (sum over layers and
+(b, h) of the rows each call scores and selects from), with the dominant
+kernel's achieved HBM GB/s against the measured copy bandwidth.
+
+Other workloads (--workload): decode (B=32, H=8, 2048 prefill then
+single-token steps, budget 512, recent 128), long_context (B=4, H=8,
+16 x 8192-token blocks, budget 4096), knorm_single (B=H=1, fp32, S=1024).
+
+Arms:
+  --impl ours       (default) libevict on the GPU
+  --impl reference  the CPU oracle (numpy), as it stands, on a bounded sample
+                    of the same workload; prints the same JSON line.
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload on its
+own GPU (independent units, no collective on the data path); value is the
+sum over ranks divided by the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kv_cache_token_bf16_gb300 import synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "cache tokens evicted-and-compacted/sec per layer; achieved HBM GB/s vs roofline"
+UNIT = "tokens/s"
+
+
+# ----------------------------------------------------------------------------
+# workloads
+# ----------------------------------------------------------------------------
+WORKLOADS = {
+    "qfilters_stack": dict(method="qfilters", layers=28, batch=1, heads=8, q_heads=24, seq=8192, budget=1024,
+                           n_sink=4, recent=0, dtype="bf16"),
+    "decode": dict(method="knorm", layers=1, batch=32, heads=8, prefill=2048, steps=256, budget=512, n_sink=4,
+                   recent=128, dtype="bf16"),
+    "long_context": dict(method="knorm", layers=1, batch=4, heads=8, block=8192, blocks=16, budget=4096, n_sink=4,
+                         recent=0, dtype="bf16"),
+    "knorm_single": dict(method="knorm", layers=1, batch=1, heads=1, seq=1024, budget=512, n_sink=4, recent=0,
+                         dtype="fp32"),
+}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "kv_cache_token_bf16_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_hash") != _source_hash(*rec.get("sources", [])):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+class StackRun:
+    """Q-Filters layer stack: 28 caches updated by one grouped call per step."""
+
+    def __init__(self, w, torch, binding, stream):
+        self.w, self.torch, self.binding = w, torch, binding
+        L, H, S = w["layers"], w["heads"], w["seq"]
+        self.k, self.v, self.q = [], [], []
+        self.filters = []
+        for layer in range(L):
+            d = synth.qfilters_layer(layer, n_q_heads=w["q_heads"], n_kv_heads=H, seq_len=S, batch=w["batch"])
+            self.k.append(torch.from_numpy(d["k"].view(np.int16)).cuda().view(torch.bfloat16))
+            self.v.append(torch.from_numpy(d["v"].view(np.int16)).cuda().view(torch.bfloat16))
+            qd = torch.from_numpy(d["queries"].view(np.int16)).cuda()
+            f = torch.empty((H, 128), dtype=torch.float32, device="cuda")
+            t0 = time.perf_counter()
+            binding.evict_qfilters_calibrate(qd.data_ptr(), binding.EVICT_BF16, w["q_heads"], qd.shape[1], 128, H,
+                                             f.data_ptr(), stream.cuda_stream)
+            self.calib_ms = (time.perf_counter() - t0) * 1e3
+            self.filters.append(f)
+        self.caches = [binding.EvictCache("qfilters", w["batch"], H, budget=w["budget"], n_sink=w["n_sink"],
+                                          recent=w["recent"], max_block=S, filters=f, sign=1,
+                                          stream=stream.cuda_stream) for f in self.filters]
+        self.handles = [c.handle for c in self.caches]
+        self.kp = [t.data_ptr() for t in self.k]
+        self.vp = [t.data_ptr() for t in self.v]
+        self.tokens_per_step = L * w["batch"] * H * S
+        self.calls_per_step = 1
+
+    def step(self):
+        for h in self.handles:
+            self.binding.evict_reset(h)
+        self.binding.evict_update_and_fetch_group(self.handles, self.kp, self.vp, None, self.w["seq"])
+
+    # end-to-end through the public host-buffer call: inputs start in pinned host memory
+    def setup_e2e(self):
+        torch = self.torch
+        self.kh = [t.view(torch.int16).cpu().pin_memory() for t in self.k]
+        self.vh = [t.view(torch.int16).cpu().pin_memory() for t in self.v]
+        n = self.w["batch"] * self.w["heads"] * self.w["budget"]
+        self.out_h = torch.empty((len(self.caches), n), dtype=torch.int32).pin_memory()
+        self.h2d = sum(t.numel() * 2 for t in self.kh) + sum(t.numel() * 2 for t in self.vh)
+        self.d2h = self.out_h.numel() * 4
+
+    def step_e2e(self):
+        torch = self.torch
+        for i, h in enumerate(self.handles):
+            self.binding.evict_reset(h)
+            view = self.binding.evict_update_and_fetch_host(h, self.kh[i].data_ptr(), self.vh[i].data_ptr(), None,
+                                                            self.w["seq"])
+            pos = self.binding.view_tensors(view, self.w["batch"], self.w["heads"], "bf16")[2]
+            self.out_h[i].copy_(pos.reshape(-1), non_blocking=True)
+
+    def score_bytes_per_launch(self):
+        w = self.w
+        return w["layers"] * w["batch"] * w["heads"] * w["seq"] * (128 * 2 + 4)
+
+
+class DecodeRun:
+    """Decode streaming: after a 2048-token prefill, one step = one single-token update."""
+
+    def __init__(self, w, torch, binding, stream):
+        self.w, self.torch, self.binding = w, torch, binding
+        B, H = w["batch"], w["heads"]
+        k0, v0 = synth.decode_prefill(B, H, w["prefill"])
+        self.k0 = torch.from_numpy(k0.view(np.int16)).cuda().view(torch.bfloat16)
+        self.v0 = torch.from_numpy(v0.view(np.int16)).cuda().view(torch.bfloat16)
+        ks, vs = synth.decode_steps(0, w["steps"], B, H)
+        self.ks = torch.from_numpy(ks.view(np.int16)).cuda().view(torch.bfloat16)
+        self.vs = torch.from_numpy(vs.view(np.int16)).cuda().view(torch.bfloat16)
+        self.cache = binding.EvictCache(w["method"], B, H, budget=w["budget"], n_sink=w["n_sink"],
+                                        recent=w["recent"], max_block=w["prefill"], stream=stream.cuda_stream)
+        self.handle = self.cache.handle
+        self.handles = [self.handle]
+        self.cache.update_and_fetch(self.k0, self.v0)
+        self.i = 0
+        self.tokens_per_step = B * H * (w["budget"] + 1)
+        self.calls_per_step = 1
+
+    def step(self):
+        s = self.i % self.w["steps"]
+        self.binding.evict_update_and_fetch(self.handle, self.ks[s].data_ptr(), self.vs[s].data_ptr(), None, 1)
+        self.i += 1
+
+    def setup_e2e(self):
+        t = self.torch
+        self.kh = self.ks.view(t.int16).cpu().pin_memory()
+        self.vh = self.vs.view(t.int16).cpu().pin_memory()
+        self.out_h = t.empty((self.w["batch"] * self.w["heads"] * self.w["budget"],), dtype=t.int32).pin_memory()
+        self.h2d = 2 * self.kh[0].numel() * 2
+        self.d2h = self.out_h.numel() * 4
+
+    def step_e2e(self):
+        s = self.i % self.w["steps"]
+        view = self.binding.evict_update_and_fetch_host(self.handle, self.kh[s].data_ptr(), self.vh[s].data_ptr(),
+                                                        None, 1)
+        self.i += 1
+        pos = self.binding.view_tensors(view, self.w["batch"], self.w["heads"], "bf16")[2]
+        self.out_h.copy_(pos.reshape(-1), non_blocking=True)
+
+    def score_bytes_per_launch(self):
+        w = self.w
+        return w["batch"] * w["heads"] * (128 * 2 + 4)
+
+
+class LongContextRun:
+    """Long-context chunked prefill: one step = 16 blocks of 8192 tokens through one cache."""
+
+    def __init__(self, w, torch, binding, stream):
+        self.w, self.torch, self.binding = w, torch, binding
+        B, H = w["batch"], w["heads"]
+        self.k, self.v = [], []
+        for blk in range(w["blocks"]):
+            k, v = synth.long_context_block(blk, B, H, w["block"])
+            self.k.append(torch.from_numpy(k.view(np.int16)).cuda().view(torch.bfloat16))
+            self.v.append(torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16))
+        self.cache = binding.EvictCache(w["method"], B, H, budget=w["budget"], n_sink=w["n_sink"],
+                                        recent=w["recent"], max_block=w["block"], stream=stream.cuda_stream)
+        self.handle = self.cache.handle
+        self.handles = [self.handle]
+        per_bh = sum(min(blk * w["block"], w["budget"]) + w["block"] for blk in range(w["blocks"]))
+        self.tokens_per_step = B * H * per_bh
+        self.calls_per_step = w["blocks"]
+
+    def step(self):
+        self.binding.evict_reset(self.handle)
+        for k, v in zip(self.k, self.v):
+            self.binding.evict_update_and_fetch(self.handle, k.data_ptr(), v.data_ptr(), None, self.w["block"])
+
+    def setup_e2e(self):
+        t = self.torch
+        self.kh = [x.view(t.int16).cpu().pin_memory() for x in self.k]
+        self.vh = [x.view(t.int16).cpu().pin_memory() for x in self.v]
+        self.out_h = t.empty((self.w["batch"] * self.w["heads"] * self.w["budget"],), dtype=t.int32).pin_memory()
+        self.h2d = sum(x.numel() * 2 for x in self.kh) * 2
+        self.d2h = self.out_h.numel() * 4
+
+    def step_e2e(self):
+        self.binding.evict_reset(self.handle)
+        view = None
+        for kh, vh in zip(self.kh, self.vh):
+            view = self.binding.evict_update_and_fetch_host(self.handle, kh.data_ptr(), vh.data_ptr(), None,
+                                                            self.w["block"])
+        pos = self.binding.view_tensors(view, self.w["batch"], self.w["heads"], "bf16")[2]
+        self.out_h.copy_(pos.reshape(-1), non_blocking=True)
+
+    def score_bytes_per_launch(self):
+        w = self.w
+        return w["batch"] * w["heads"] * w["block"] * (128 * 2 + 4)
+
+
+class KnormSingleRun:
+    def __init__(self, w, torch, binding, stream):
+        self.w, self.torch, self.binding = w, torch, binding
+        k, v = synth.knorm_single_sequence(w["seq"])
+        self.k, self.v = torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda()
+        self.cache = binding.EvictCache("knorm", 1, 1, budget=w["budget"], n_sink=w["n_sink"], recent=0,
+                                        max_block=w["seq"], dtype="fp32", stream=stream.cuda_stream)
+        self.handle = self.cache.handle
+        self.handles = [self.handle]
+        self.tokens_per_step = w["seq"]
+        self.calls_per_step = 1
+
+    def step(self):
+        self.binding.evict_reset(self.handle)
+        self.binding.evict_update_and_fetch(self.handle, self.k.data_ptr(), self.v.data_ptr(), None, self.w["seq"])
+
+    def setup_e2e(self):
+        t = self.torch
+        self.kh, self.vh = self.k.cpu().pin_memory(), self.v.cpu().pin_memory()
+        self.out_h = t.empty((self.w["budget"],), dtype=t.int32).pin_memory()
+        self.h2d, self.d2h = 2 * self.kh.numel() * 4, self.out_h.numel() * 4
+
+    def step_e2e(self):
+        self.binding.evict_reset(self.handle)
+        view = self.binding.evict_update_and_fetch_host(self.handle, self.kh.data_ptr(), self.vh.data_ptr(), None,
+                                                        self.w["seq"])
+        pos = self.binding.view_tensors(view, 1, 1, "fp32")[2]
+        self.out_h.copy_(pos.reshape(-1), non_blocking=True)
+
+    def score_bytes_per_launch(self):
+        return self.w["seq"] * (128 * 4 + 4)
+
+
+RUNS = {"qfilters_stack": StackRun, "decode": DecodeRun, "long_context": LongContextRun,
+        "knorm_single": KnormSingleRun}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from kv_cache_token_bf16_gb300 import binding
+    stream = torch.cuda.Stream()
+    w = WORKLOADS[args.workload]
+    with torch.cuda.stream(stream):
+        run = RUNS[args.workload](w, torch, binding, stream)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up
+    for _ in range(args.warmup):
+        run.step()
+    barrier()
+    # timed region: device time with CUDA events on the launching stream; the
+    # first handle records per-kernel events on the same stream for the roofline
+    for h in run.handles[:1]:
+        binding.evict_set_profiling(h, True)
+    launches0 = binding.evict_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            run.step()
+        ev1.record(stream)
+        barrier()
+    launches = binding.evict_launch_count() - launches0
+    ms = ev0.elapsed_time(ev1)
+    ktimes = binding.evict_kernel_times(run.handles[0])
+    binding.evict_set_profiling(run.handles[0], False)
+    for h in run.handles:
+        binding.evict_sync(h)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * run.tokens_per_step / (ms_per_step / 1e3)
+
+    # end-to-end through the host-buffer entry point (copies inside the region)
+    run.setup_e2e()
+    for _ in range(min(args.warmup, 3)):
+        run.step_e2e()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        run.step_e2e()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peak, peak_kind = _peaks()
+    alg_bytes = algorithmic_bytes(run, binding)
+    kernels = {}
+    tot = sum(t for _, t in ktimes.values())
+    for k, (n, t) in ktimes.items():
+        kernels[k] = {"launches": n, "avg_us": round(t / n * 1e3, 2), "share": round(t / tot, 4) if tot else None}
+        if k in alg_bytes:
+            kernels[k]["algorithmic_bytes_per_launch"] = alg_bytes[k]
+            kernels[k]["achieved_gbs"] = round(alg_bytes[k] / (t / n / 1e3) / 1e9, 1)
+    roof = None
+    if ktimes:
+        top = max(ktimes, key=lambda k: ktimes[k][1])
+        n_launch, tot_ms = ktimes[top]
+        per_launch_ms = tot_ms / n_launch
+        alg = alg_bytes.get(top)
+        achieved = alg / (per_launch_ms / 1e3) / 1e9 if alg else None
+        roof = {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
+                "peak": peak, "peak_kind": peak_kind + " (HBM copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback", "unit": "GB/s",
+                "frac": round(achieved / peak, 4) if achieved else None,
+                "traffic": _ncu_traffic(top, args.workload), "algorithmic_bytes_per_launch": alg,
+                "avg_launch_us": round(per_launch_ms * 1e3, 2)}
+    cpu = cpu_baseline(args.workload) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generators standing in for real-model activations)",
+            "config": {"workload": args.workload, **{k: v for k, v in w.items()},
+                       "storage": w["dtype"], "tokens_per_step": run.tokens_per_step,
+                       "calls_per_step": run.calls_per_step, "l2": "inputs larger than L2" if
+                       args.workload in ("qfilters_stack", "long_context") else "working set may be L2-resident",
+                       "parallelism": f"replica-per-gpu x{world}"},
+            "e2e": {"value": round(world * run.tokens_per_step / (e2e_ms / 1e3), 1), "unit": UNIT,
+                    "h2d_bytes_per_step": run.h2d, "d2h_bytes_per_step": run.d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": int(launches),
+            "roofline": roof,
+            "kernels": kernels,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        if hasattr(run, "calib_ms"):
+            line["config"]["calibration_ms_per_layer"] = round(run.calib_ms, 3)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def algorithmic_bytes(run, binding):
+    """Bytes each kernel must move per launch (one launch covers every layer of a call).
+
+    score    : read each incoming key once, write its fp32 score.
+    select   : read the n scores of every (b, h), write the budget-long source
+               map, reset the chunk flags, write the 8-byte metadata.
+    compact  : per incoming survivor read K and V, write K, V, position and
+               score, read its score and map entry (4*D*e + 16 bytes); per kept
+               row whose slot changes read and write K, V, position and score
+               and read its map entry (4*D*e + 20 bytes). Rows counted from
+               the last call (evict_compaction_rows).
+    """
+    w = run.w
+    e = 2 if w["dtype"] == "bf16" else 4
+    units = w["layers"] * w["batch"] * w["heads"]
+    out = {}
+    m = w.get("seq", w.get("block", 1))
+    if isinstance(run, DecodeRun):
+        m = 1
+    out["score"] = units * m * (128 * e + 4)
+    old, new = 0, 0
+    for h in run.handles:
+        a, b = binding.evict_compaction_rows(h)
+        old, new = old + a, new + b
+    out["compact"] = new * (4 * 128 * e + 16) + old * (4 * 128 * e + 20)
+    n = w["budget"] + m if not isinstance(run, StackRun) else m
+    flag_stride = -(-w["budget"] // (32 if e == 2 else 16))
+    out["select"] = units * (4 * n + 4 * w["budget"] + 4 * flag_stride + 8)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ----------------------------------------------------------------------------
+def _oracle_sample(workload, budget_s=10.0):
+    """Run the oracle on a bounded sample of the workload; returns (tokens, seconds, description)."""
+    from oracle import calibrate as ocal
+    from oracle.cache import OracleCache
+    w = WORKLOADS[workload]
+    tokens, secs, done = 0, 0.0, 0
+    if workload == "qfilters_stack":
+        t0 = time.perf_counter()
+        for layer in range(w["layers"]):
+            d = synth.qfilters_layer(layer, seq_len=w["seq"])
+            t1 = time.perf_counter()
+            f = ocal.calibrate(d["queries"], w["heads"]).astype(np.float32)
+            c = OracleCache("qfilters", w["batch"], w["heads"], budget=w["budget"], n_sink=w["n_sink"],
+                            recent=w["recent"], filters=f)
+            t2 = time.perf_counter()                       # calibration is off the per-step path
+            c.update_and_fetch(d["k"], d["v"])
+            secs += time.perf_counter() - t2
+            tokens += w["batch"] * w["heads"] * w["seq"]
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        return tokens, secs, f"{done} of {w['layers']} layers (one prefill update each; calibration untimed)"
+    if workload == "decode":
+        k0, v0 = synth.decode_prefill(w["batch"], w["heads"], w["prefill"])
+        c = OracleCache(w["method"], w["batch"], w["heads"], budget=w["budget"], n_sink=w["n_sink"],
+                        recent=w["recent"])
+        c.update_and_fetch(k0, v0)
+        ks, vs = synth.decode_steps(0, 64, w["batch"], w["heads"])
+        t0 = time.perf_counter()
+        for s in range(64):
+            c.update_and_fetch(ks[s], vs[s])
+            tokens += w["batch"] * w["heads"] * (w["budget"] + 1)
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        return tokens, time.perf_counter() - t0, f"{done} decode steps after the 2048-token prefill"
+    if workload == "long_context":
+        c = OracleCache(w["method"], w["batch"], w["heads"], budget=w["budget"], n_sink=w["n_sink"],
+                        recent=w["recent"])
+        for blk in range(w["blocks"]):
+            k, v = synth.long_context_block(blk, w["batch"], w["heads"], w["block"])
+            t1 = time.perf_counter()
+            n = c.n_kept + w["block"]
+            c.update_and_fetch(k, v)
+            secs += time.perf_counter() - t1
+            tokens += w["batch"] * w["heads"] * n
+            done += 1
+            if secs > budget_s:
+                break
+        return tokens, secs, f"{done} of {w['blocks']} blocks"
+    k, v = synth.knorm_single_sequence(w["seq"])
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < min(budget_s, 2.0):
+        c = OracleCache("knorm", 1, 1, budget=w["budget"], n_sink=w["n_sink"], dtype="fp32")
+        c.update_and_fetch(k, v)
+        tokens += w["seq"]
+        done += 1
+    return tokens, time.perf_counter() - t0, f"{done} one-block prefills"
+
+
+def cpu_baseline(workload):
+    tokens, secs, sample = _oracle_sample(workload)
+    return {"value": round(tokens / secs, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": sample + "; numpy, single thread (the oracle's array ops do not use BLAS threads)"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    vals = []
+    for _ in range(args.warmup):
+        _oracle_sample(args.workload, budget_s=2.0)
+    tokens_total, secs_total, sample = 0, 0.0, ""
+    for _ in range(args.steps):
+        t, s, sample = _oracle_sample(args.workload, budget_s=5.0)
+        tokens_total += t
+        secs_total += s
+        vals.append(t / s)
+    value = tokens_total / secs_total
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs_total / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": args.workload, **w},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qfilters_stack")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

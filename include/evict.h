@@ -204,6 +204,13 @@ typedef struct evict_kernel_time {
  * to max_entries of them to out; *n_out receives the number written. */
 int evict_kernel_times(evict_handle* h, evict_kernel_time* out, int max_entries, int* n_out);
 
+/* Rows moved by the handle's last over-budget update, summed over (b,h):
+ * *old_moved = kept rows that changed slot, *new_written = incoming rows
+ * written into the cache. Synchronises the stream (diagnostic; used to
+ * count the compaction's algorithmic bytes). Both are 0 if the last update
+ * appended without eviction. */
+int evict_compaction_rows(evict_handle* h, int64_t* old_moved, int64_t* new_written);
+
 /* Process-wide count of kernels this library has launched. */
 int64_t evict_launch_count(void);
 

@@ -77,6 +77,7 @@ _SIGNATURES = {
     "evict_qfilters_calibrate": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "evict_set_profiling": (_I, [_P, _I]),
     "evict_kernel_times": (_I, [_P, ctypes.POINTER(EvictKernelTime), _I, ctypes.POINTER(_I)]),
+    "evict_compaction_rows": (_I, [_P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "evict_launch_count": (ctypes.c_int64, []),
     "evict_last_error": (ctypes.c_char_p, []),
 }
@@ -184,6 +185,12 @@ def evict_kernel_times(h) -> dict:
     n = _I()
     check(load().evict_kernel_times(h, buf, 32, ctypes.byref(n)))
     return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n.value)}
+
+
+def evict_compaction_rows(h):
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    check(load().evict_compaction_rows(h, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 def evict_launch_count() -> int:

@@ -64,6 +64,7 @@ struct evict_handle {
 
   int n_kept = 0;             // rows per (b, h), identical for every (b, h)
   int64_t offset = 0;         // absolute position of the next token
+  bool last_evicted = false;  // the last update ran select + compaction
 
   bool profiling = false;
   struct Rec {

@@ -213,7 +213,10 @@ int run_intrinsic(evict_handle* const* hs, int n_layers, const void* const* k, c
   if (n <= h->cfg.budget) {
     e = timed_launch(h, kKidAppend, [&] { return launch_append(P, h->elem, h->stream); });
     if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
-    for (int l = 0; l < n_layers; ++l) hs[l]->n_kept = (int)n;
+    for (int l = 0; l < n_layers; ++l) {
+      hs[l]->n_kept = (int)n;
+      hs[l]->last_evicted = false;
+    }
   } else {
     e = timed_launch(h, kKidScore, [&] { return launch_score(P, h->elem, h->stream); });
     if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
@@ -221,7 +224,10 @@ int run_intrinsic(evict_handle* const* hs, int n_layers, const void* const* k, c
     if (e != cudaSuccess) return cuda_fail(e, "select kernel launch");
     e = timed_launch(h, kKidCompact, [&] { return launch_compact(P, h->elem, h->stream); });
     if (e != cudaSuccess) return cuda_fail(e, "compact kernel launch");
-    for (int l = 0; l < n_layers; ++l) hs[l]->n_kept = h->cfg.budget;
+    for (int l = 0; l < n_layers; ++l) {
+      hs[l]->n_kept = h->cfg.budget;
+      hs[l]->last_evicted = true;
+    }
   }
   for (int l = 0; l < n_layers; ++l) hs[l]->offset += m;
   return EVICT_OK;
@@ -403,6 +409,7 @@ int evict_set_state(evict_handle* h, const void* k, const void* v, const int32_t
   }
   h->n_kept = n;
   h->offset = offset;
+  h->last_evicted = false;
   return EVICT_OK;
 }
 
@@ -410,6 +417,7 @@ int evict_reset(evict_handle* h) {
   if (!h) return fail(EVICT_EINVAL, "handle is NULL");
   h->n_kept = 0;
   h->offset = 0;
+  h->last_evicted = false;
   return EVICT_OK;
 }
 
@@ -476,6 +484,23 @@ int evict_kernel_times(evict_handle* h, evict_kernel_time* out, int max_entries,
     }
   }
   *n_out = n;
+  return EVICT_OK;
+}
+
+int evict_compaction_rows(evict_handle* h, int64_t* old_moved, int64_t* new_written) {
+  if (!h || !old_moved || !new_written) return fail(EVICT_EINVAL, "arguments must not be NULL");
+  *old_moved = 0;
+  *new_written = 0;
+  if (!h->last_evicted) return EVICT_OK;
+  const size_t bh = (size_t)h->cfg.batch * h->cfg.n_kv_heads;
+  std::vector<int2> meta(bh);
+  cudaError_t e = cudaStreamSynchronize(h->stream);
+  if (e == cudaSuccess) e = cudaMemcpy(meta.data(), h->meta, bh * sizeof(int2), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading compaction metadata");
+  for (const int2& m : meta) {
+    *old_moved += m.y - m.x;
+    *new_written += h->cfg.budget - m.y;
+  }
   return EVICT_OK;
 }
 
