@@ -274,7 +274,7 @@ int evict_init(const evict_config* cfg, evict_handle** out) {
     return cuda_fail(err, what);
   };
   if ((e = cudaMemsetAsync(h->arena, 0, bytes, h->stream)) != cudaSuccess) return bail(e, "clearing the cache");
-  if ((e = prepare_select(h->cap + cfg->max_block)) != cudaSuccess) return bail(e, "select kernel attribute");
+  if ((e = prepare_select()) != cudaSuccess) return bail(e, "select kernel attribute");
   if (cfg->method == EVICT_QFILTERS) {
     const size_t fb = (size_t)cfg->n_kv_heads * kHeadDim * sizeof(float);
     if ((e = cudaMemcpyAsync(h->filters, cfg->filters, fb, cudaMemcpyDeviceToDevice, h->stream)) != cudaSuccess)

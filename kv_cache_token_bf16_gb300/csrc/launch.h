@@ -12,8 +12,9 @@ int compact_chunk_rows(int dtype_bytes);
 
 cudaError_t launch_score(const GroupParams& P, int dtype_bytes, cudaStream_t st);
 cudaError_t launch_append(const GroupParams& P, int dtype_bytes, cudaStream_t st);
-// Raise the select kernel's dynamic shared memory limit to hold max_rows keys.
-cudaError_t prepare_select(int max_rows);
+// Raise the select kernel's dynamic shared memory limit (current device) to
+// hold EVICT_MAX_SELECT_ROWS keys.
+cudaError_t prepare_select();
 cudaError_t launch_select(const GroupParams& P, cudaStream_t st);
 // Sets P.total_ctas.
 cudaError_t launch_compact(GroupParams& P, int dtype_bytes, cudaStream_t st);

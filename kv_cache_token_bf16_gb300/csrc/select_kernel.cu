@@ -5,6 +5,7 @@
 // unprotected rows by priority; rows strictly above the cutoff are always
 // admitted and rows equal to it only while quota remains, lowest index first,
 // so the budget is never exceeded.
+#include "../../include/evict.h"
 #include "common.cuh"
 #include "launch.h"
 #include "params.h"
@@ -169,9 +170,11 @@ cudaError_t launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream
 
 }  // namespace
 
-cudaError_t prepare_select(int max_rows) {
+cudaError_t prepare_select() {
+  // Always the compiled maximum: the attribute is per function and device, so
+  // a smaller value set for one cache would break launches of a larger one.
   return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)(max_rows * sizeof(uint32_t)));
+                              (int)(EVICT_MAX_SELECT_ROWS * sizeof(uint32_t)));
 }
 
 cudaError_t launch_select(const GroupParams& P, cudaStream_t st) {
