@@ -290,3 +290,14 @@ def test_long_context_full_size_sampled_units(method):
             assert np.array_equal(gk[b, h], ref.k[0, 0]) and np.array_equal(gv[b, h], ref.v[0, 0])
             assert gs[b, h].tobytes() == ref.score[0, 0].tobytes()
     assert gpu.stats()["offset"] == blocks * 8192
+
+
+def test_small_cache_created_after_a_large_one_does_not_break_it():
+    # the select kernel's shared-memory limit is per function, not per cache
+    from kv_cache_token_bf16_gb300 import binding
+    k, v = synth.gaussian_block(15, 1, 2, 8192)
+    gpu, ref = _pair("knorm", 1, 2, 4096, n_sink=4)
+    small = binding.EvictCache("knorm", 1, 1, budget=16, n_sink=1, max_block=16)
+    view = _feed(gpu, ref, k, v, [0, 8192])
+    assert_cache_equal(view, ref, "large after small")
+    small.close()
