@@ -26,7 +26,7 @@ def test_leverage_on_a_known_decomposition():
 
 
 def test_full_rank_leverage_is_row_energy_share():
-    # spec identity: summed over all directions, l_i = ||w_i||^2 / ||W||_F^2
+    # summed over every singular direction the leverage of row i is ||w_i||^2 / ||W||_F^2
     g = synth.rng(52)
     w = g.standard_normal((500, 128)) * g.uniform(0, 3, (500, 1))
     l = curdkv.leverage(w, 128)
