@@ -156,6 +156,34 @@ int evict_update_and_fetch_host(evict_handle* h, const void* k_host, const void*
 /* The current kept cache (no work enqueued). */
 int evict_get_view(const evict_handle* h, evict_view* out);
 
+/* One-shot KNorm / Q-Filters eviction of a single block that allocates
+ * nothing. The pages have no counterpart to this call; it exists for callers
+ * that cannot call cudaMalloc: code running while a CUDA graph is being
+ * captured, serving runtimes that reserve all device memory in their own
+ * pool at start-up and forbid later allocations, and plug-ins living inside
+ * another framework's memory manager.
+ *
+ * Same result as a fresh cache created with `cfg` absorbing k, v once
+ * through evict_update_and_fetch (offset 0), written to caller buffers:
+ *   k, v       [B, H, n, D] device inputs; pos [B, n] device int32 or NULL
+ *              (positions 0..n-1); cfg->filters is read in place (not copied);
+ *   k_out, v_out [B, H, budget, D], pos_out, score_out [B, H, budget]
+ *              device outputs; rows [0, min(n, budget)) of each (b,h) are
+ *              written in temporal order.
+ * cfg->max_block, max_kept and rank_cap are ignored; work goes on cfg->stream
+ * and the call returns without synchronising.
+ * Intermediate data lives in one fixed 8 MiB device array inside the library
+ * (held by every GPU that loads it until process exit). A call needs
+ * B*H*(4n + 4*budget + 8 + 4*ceil(budget/chunk)) bytes of it plus small
+ * rounding (chunk = 32 rows for bf16, 16 for fp32); larger calls return
+ * EVICT_ELIMIT. The first call on a device looks up the array's address with
+ * that device current — make it before any stream capture. All calls on a
+ * device share the array, so calls that overlap on the GPU race.
+ *   EVICT_EINVAL  bad configuration (as evict_init), CurDKV, NULL pointers;
+ *   EVICT_ELIMIT  scratch or row bound exceeded;  EVICT_ECUDA  launch failure. */
+int evict_prefill_noalloc(const evict_config* cfg, const void* k, const void* v, const int32_t* pos, int n,
+                          void* k_out, void* v_out, int32_t* pos_out, float* score_out);
+
 /* Byte accounting from host-side counters (never synchronises). */
 int evict_stats(const evict_handle* h, evict_stats_t* out);
 

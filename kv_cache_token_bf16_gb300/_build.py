@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libevict.so")
 
-SOURCES = ["score_kernels.cu", "select_kernel.cu", "compact_kernel.cu", "evict_api.cu", "calib.cu", "curdkv.cu"]
+SOURCES = ["score_kernels.cu", "select_kernel.cu", "compact_kernel.cu", "evict_api.cu", "calib.cu", "curdkv.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

@@ -78,6 +78,7 @@ _SIGNATURES = {
     "evict_set_profiling": (_I, [_P, _I]),
     "evict_kernel_times": (_I, [_P, ctypes.POINTER(EvictKernelTime), _I, ctypes.POINTER(_I)]),
     "evict_compaction_rows": (_I, [_P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
+    "evict_prefill_noalloc": (_I, [ctypes.POINTER(EvictConfig), _P, _P, _P, _I, _P, _P, _P, _P]),
     "evict_launch_count": (ctypes.c_int64, []),
     "evict_last_error": (ctypes.c_char_p, []),
 }
@@ -191,6 +192,12 @@ def evict_compaction_rows(h):
     a, b = ctypes.c_int64(), ctypes.c_int64()
     check(load().evict_compaction_rows(h, ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value
+
+
+def evict_prefill_noalloc(cfg: EvictConfig, k_ptr, v_ptr, pos_ptr, n, k_out, v_out, pos_out, score_out):
+    """One-shot block eviction into caller buffers with no device allocation."""
+    check(load().evict_prefill_noalloc(ctypes.byref(cfg), k_ptr, v_ptr, pos_ptr, n, k_out, v_out, pos_out,
+                                       score_out))
 
 
 def evict_launch_count() -> int:
