@@ -239,6 +239,13 @@ int evict_kernel_times(evict_handle* h, evict_kernel_time* out, int max_entries,
  * appended without eviction. */
 int evict_compaction_rows(evict_handle* h, int64_t* old_moved, int64_t* new_written);
 
+/* CurDKV diagnostics: copy the last update's proxy-attention column sums
+ * and leverage of every row of the concatenation (kept rows first, then the
+ * block; before compaction) to device buffers attn, leverage [B, H, n]
+ * (either may be NULL); *n_rows receives n (0 before the first update).
+ * Enqueued on the handle's stream. EVICT_EINVAL for other methods. */
+int evict_curdkv_scores(evict_handle* h, float* attn, float* leverage, int* n_rows);
+
 /* Process-wide count of kernels this library has launched. */
 int64_t evict_launch_count(void);
 

@@ -110,9 +110,15 @@ cudaError_t timed_launch(evict_handle* h, int kid, F&& f) {
   return e;
 }
 
+// Launch parameters of an update of n_layers same-shaped caches (evict_api.cu).
+GroupParams make_group_params(const evict_handle* h, int m, int n_layers);
+LayerPtrs make_layer_ptrs(evict_handle* h, const void* k, const void* v, const int32_t* pos);
+
 // CurDKV hooks (curdkv.cu).
 void curdkv_layout(evict_handle* h, size_t* offset, char* base);
+void curdkv_release(evict_handle* h);
 int curdkv_prepare(evict_handle* h);
 int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* pos, int m);
+int curdkv_last_scores(const evict_handle* h, float* attn, float* lev, int* n_out);
 
 }  // namespace evict

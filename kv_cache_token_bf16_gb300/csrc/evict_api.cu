@@ -143,7 +143,11 @@ int validate(const evict_config* c) {
   return EVICT_OK;
 }
 
-GroupParams base_params(const evict_handle* h, int m, int n_layers) {
+}  // namespace
+
+namespace evict {
+
+GroupParams make_group_params(const evict_handle* h, int m, int n_layers) {
   GroupParams P;
   memset(&P, 0, sizeof(P));
   const evict_config& c = h->cfg;
@@ -167,7 +171,7 @@ GroupParams base_params(const evict_handle* h, int m, int n_layers) {
   return P;
 }
 
-LayerPtrs layer_ptrs(evict_handle* h, const void* k, const void* v, const int32_t* pos) {
+LayerPtrs make_layer_ptrs(evict_handle* h, const void* k, const void* v, const int32_t* pos) {
   LayerPtrs L;
   L.k_in = k;
   L.v_in = v;
@@ -183,6 +187,10 @@ LayerPtrs layer_ptrs(evict_handle* h, const void* k, const void* v, const int32_
   L.flags = h->flags;
   return L;
 }
+
+}  // namespace evict
+
+namespace {
 
 void fill_view(const evict_handle* h, evict_view* out) {
   if (!out) return;
@@ -206,8 +214,8 @@ bool same_shape(const evict_handle* a, const evict_handle* b) {
 int run_intrinsic(evict_handle* const* hs, int n_layers, const void* const* k, const void* const* v,
                   const int32_t* const* pos, int m) {
   evict_handle* h = hs[0];
-  GroupParams P = base_params(h, m, n_layers);
-  for (int l = 0; l < n_layers; ++l) P.L[l] = layer_ptrs(hs[l], k[l], v[l], pos ? pos[l] : nullptr);
+  GroupParams P = make_group_params(h, m, n_layers);
+  for (int l = 0; l < n_layers; ++l) P.L[l] = make_layer_ptrs(hs[l], k[l], v[l], pos ? pos[l] : nullptr);
   const long long n = (long long)h->n_kept + m;
   cudaError_t e;
   if (n <= h->cfg.budget) {
@@ -295,6 +303,7 @@ int evict_init(const evict_config* cfg, evict_handle** out) {
     rc = curdkv_prepare(h);
     if (rc) {
       cudaFree(h->arena);
+      curdkv_release(h);
       delete h;
       return rc;
     }
@@ -452,6 +461,7 @@ void evict_destroy(evict_handle* h) {
   }
   for (auto ev : h->event_pool) cudaEventDestroy(ev);
   cudaFree(h->arena);
+  curdkv_release(h);
   delete h;
 }
 
@@ -502,6 +512,12 @@ int evict_compaction_rows(evict_handle* h, int64_t* old_moved, int64_t* new_writ
     *new_written += h->cfg.budget - m.y;
   }
   return EVICT_OK;
+}
+
+int evict_curdkv_scores(evict_handle* h, float* attn, float* leverage, int* n_rows) {
+  if (!h || !n_rows) return fail(EVICT_EINVAL, "handle and n_rows must not be NULL");
+  if (h->cfg.method != EVICT_CURDKV) return fail(EVICT_EINVAL, "not a CurDKV cache");
+  return curdkv_last_scores(h, attn, leverage, n_rows);
 }
 
 int64_t evict_launch_count(void) { return g_launches.load(); }

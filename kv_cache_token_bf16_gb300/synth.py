@@ -223,3 +223,30 @@ def gaussian_block(seed: int, batch: int, n_kv_heads: int, length: int, dtype: s
     if dtype == "bf16":
         return f32_to_bf16_bits(k), f32_to_bf16_bits(v)
     return k, v
+
+
+def planted_spectrum_values(seed: int, batch: int, n_kv_heads: int, length: int, rank: int = 16,
+                            top: float = 3.0, decay: float = 0.9, floor: float = 0.05):
+    """Values whose rows share a planted spectrum: V = Z diag(s) R^T (bf16 bits).
+
+    Z ~ N(0,1) [length, 128], R a seeded random orthogonal matrix per (b, h),
+    s_j = top * decay^j for j < rank and `floor` beyond: a clear gap after the
+    first `rank` directions.
+    """
+    g = rng(seed)
+    s = np.where(np.arange(HEAD_DIM) < rank, top * decay ** np.arange(HEAD_DIM), floor)
+    out = np.empty((batch, n_kv_heads, length, HEAD_DIM), np.float32)
+    for b in range(batch):
+        for h in range(n_kv_heads):
+            q, _ = np.linalg.qr(g.standard_normal((HEAD_DIM, HEAD_DIM)))
+            z = g.standard_normal((length, HEAD_DIM))
+            out[b, h] = (z * s) @ q.T
+    return f32_to_bf16_bits(out)
+
+
+def clustered_keys(seed: int, batch: int, n_kv_heads: int, length: int, spread: float = 0.5):
+    """Keys = a common unit direction per (b, h) + spread * N(0, I) (bf16 bits)."""
+    g = rng(seed)
+    c = unit_vectors(g, batch * n_kv_heads).reshape(batch, n_kv_heads, 1, HEAD_DIM)
+    k = c + spread * g.standard_normal((batch, n_kv_heads, length, HEAD_DIM))
+    return f32_to_bf16_bits(k.astype(np.float32))

@@ -1,0 +1,225 @@
+"""GPU parity of the CurDKV-adapted path against the CPU oracle.
+
+Compared per (b, h):
+* proxy-attention column sums: relative 1e-4 (fp32 tensor-core logits,
+  fp32 sums of ex2 terms);
+* leverage: relative 1e-3 (+ 1e-9 * sum l) wherever the oracle's rank-r
+  eigengap (lambda_{r-1} - lambda_r) / lambda_0 is at least 1e-2; below that
+  the top-r subspace itself is ill-conditioned and only the captured energy
+  (sum of leverage = sum of the top-r eigenvalue shares, well-conditioned) is
+  asserted;
+* kept sets: equal counts, and every row whose oracle priority lies more
+  than twice its tolerance from the cutoff is kept by both or by neither;
+  the compacted K/V/positions are the original rows of the kept positions.
+The oracle never receives GPU output: multi-block cases start every block
+from the oracle's own state.
+"""
+import numpy as np
+import pytest
+
+from kv_cache_token_bf16_gb300 import synth
+from oracle import curdkv as ocd
+from oracle import select as osel
+from oracle.cache import OracleCache
+from tests.gpu_util import to_bits, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+RANK = 16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _gpu_cache(B, H, budget, max_block, max_kept=0, n_sink=4, recent=0):
+    from kv_cache_token_bf16_gb300 import binding
+    return binding.EvictCache("curdkv", B, H, budget=budget, n_sink=n_sink, recent=recent, max_block=max_block,
+                              max_kept=max_kept, rank_cap=RANK)
+
+
+def _gpu_scores(cache, B, H):
+    from kv_cache_token_bf16_gb300 import binding
+    n = binding.evict_curdkv_scores(cache.handle, None, None)
+    attn = torch.empty((B, H, n), dtype=torch.float32, device="cuda")
+    lev = torch.empty_like(attn)
+    binding.evict_curdkv_scores(cache.handle, attn.data_ptr(), lev.data_ptr())
+    cache.sync()
+    return attn.cpu().numpy().astype(np.float64), lev.cpu().numpy().astype(np.float64)
+
+
+def _check_unit(k_all, v_all, m, attn_g, lev_g, cum_old, cum_g_all, kept_g, n_sink, recent, budget, what,
+                assert_lev=True):
+    """Compare one (b, h) unit with the oracle; returns the rank-r relative gap."""
+    l_or, a_or, s = ocd.block_scores(k_all, v_all, m, RANK)
+    n = len(l_or)
+    assert np.allclose(attn_g, a_or, rtol=1e-4, atol=1e-7 * m), f"{what}: attention sums"
+    lam = s ** 2
+    r = min(RANK, n, 128)
+    gap = (lam[r - 1] - lam[r]) / lam[0] if lam[0] > 0 and r < len(lam) else 1.0
+    tol = 1e-3 * l_or + 1e-9 * l_or.sum()
+    assert abs(lev_g.sum() - l_or.sum()) <= 1e-4 * l_or.sum() + 1e-12, f"{what}: captured energy"
+    if gap >= 1e-2 and assert_lev:
+        bad = np.abs(lev_g - l_or) > tol
+        assert not bad.any(), f"{what}: leverage off at {np.flatnonzero(bad)[:5]} (gap {gap:.3g})"
+    # kept set, band-tolerant around the oracle's cutoff
+    cum_or = ocd.cumulative(cum_old, l_or)
+    if n > budget:
+        kept_or = osel.kept_indices(osel.priority(cum_or)[None, None], n_sink, recent, budget)[0, 0]
+        assert len(kept_g) == budget
+        prot = osel.protected_mask(n, n_sink, recent)
+        unp = np.flatnonzero(~prot)
+        q = budget - prot.sum()
+        cutoff = np.sort(cum_or[unp])[::-1][q - 1]
+        clear = np.abs(cum_or - cutoff) > 2 * tol
+        in_or = np.isin(np.arange(n), kept_or)
+        in_g = np.isin(np.arange(n), kept_g)
+        if gap >= 1e-2 and assert_lev:
+            assert np.array_equal(in_or[clear], in_g[clear]), f"{what}: kept set differs outside the band"
+    return gap
+
+
+def _run_block(B, H, budget, k_old, v_old, cum_old, k_new, v_new, n_sink=4, recent=0, assert_lev=True,
+               units=None):
+    """One GPU update starting from the oracle-provided state; checks every (or the listed) unit."""
+    k0 = k_old.shape[2]
+    m = k_new.shape[2]
+    gpu = _gpu_cache(B, H, budget, max_block=m, max_kept=max(k0, budget), n_sink=n_sink, recent=recent)
+    if k0:
+        pos0 = np.broadcast_to(np.arange(k0, dtype=np.int32), (B, H, k0)).copy()
+        gpu.set_state(to_dev(k_old, torch), to_dev(v_old, torch), torch.from_numpy(pos0).cuda(),
+                      torch.from_numpy(cum_old.astype(np.float32)).cuda(), k0)
+    view = gpu.update_and_fetch(to_dev(k_new, torch), to_dev(v_new, torch))
+    gpu.sync()
+    attn, lev = _gpu_scores(gpu, B, H)
+    gk, gv, gp, gs = [to_bits(t) for t in view]
+    k_all = np.concatenate([k_old, k_new], axis=2)
+    v_all = np.concatenate([v_old, v_new], axis=2)
+    gaps = []
+    for b in range(B):
+        for h in range(H):
+            if units is not None and (b, h) not in units:
+                continue
+            kept = gp[b, h]
+            assert np.all(np.diff(kept) > 0)
+            assert np.array_equal(gk[b, h], k_all[b, h, kept]) and np.array_equal(gv[b, h], v_all[b, h, kept])
+            gaps.append(_check_unit(k_all[b, h], v_all[b, h], m, attn[b, h], lev[b, h],
+                                    cum_old[b, h].astype(np.float32).astype(np.float64), None, kept, n_sink,
+                                    recent, budget, f"unit {(b, h)}", assert_lev))
+    return gpu, view, attn, lev, gaps
+
+
+@pytest.mark.parametrize("k0,m,budget", [(0, 300, 64), (0, 129, 200), (500, 257, 128), (1000, 1, 64),
+                                         (127, 128, 100)])
+def test_planted_spectrum_block(k0, m, budget):
+    B, H = 1, 2
+    n = k0 + m
+    k_all = synth.clustered_keys(100 + n, B, H, n, spread=0.5)
+    v_all = synth.planted_spectrum_values(200 + n, B, H, n)
+    cum_old = synth.rng(3).uniform(0, 0.01, (B, H, k0))
+    gpu, view, attn, lev, gaps = _run_block(B, H, budget, k_all[:, :, :k0], v_all[:, :, :k0], cum_old,
+                                            k_all[:, :, k0:], v_all[:, :, k0:])
+    assert min(gaps) >= 1e-2           # the planted spectrum keeps the leverage well-conditioned
+
+
+def test_append_then_evict_accumulates_leverage():
+    # blocks of 60 into budget 200: three appends then an eviction, cumulative scores tracked
+    B, H, blk = 1, 2, 60
+    k_all = synth.clustered_keys(7, B, H, 4 * blk, spread=0.5)
+    v_all = synth.planted_spectrum_values(8, B, H, 4 * blk)
+    gpu = _gpu_cache(B, H, 200, max_block=blk)
+    ref = OracleCache("curdkv", B, H, budget=200, n_sink=4, rank_cap=RANK)
+    for c in range(4):
+        sl = slice(c * blk, (c + 1) * blk)
+        view = gpu.update_and_fetch(to_dev(k_all[:, :, sl], torch), to_dev(v_all[:, :, sl], torch))
+        ref.update_and_fetch(k_all[:, :, sl], v_all[:, :, sl])
+        gpu.sync()
+        gp, gs = to_bits(view[2]), to_bits(view[3]).astype(np.float64)
+        assert gp.shape == ref.pos.shape
+        if c < 3:
+            assert np.array_equal(gp, ref.pos)
+            assert np.allclose(gs, ref.score, rtol=2e-3, atol=1e-9), f"cumulative scores after block {c}"
+    assert gpu.stats()["offset"] == 4 * blk and gpu.stats()["tokens_kept"] == 200
+
+
+def test_zero_values_give_zero_leverage_and_index_ties():
+    B, H, n = 1, 1, 300
+    k = synth.clustered_keys(9, B, H, n)
+    v = np.zeros((B, H, n, 128), np.uint16)
+    gpu = _gpu_cache(B, H, 50, max_block=n)
+    view = gpu.update_and_fetch(to_dev(k, torch), to_dev(v, torch))
+    gpu.sync()
+    attn, lev = _gpu_scores(gpu, B, H)
+    assert np.all(lev == 0) and np.all(np.isfinite(attn))
+    assert to_bits(view[2])[0, 0].tolist() == list(range(50))     # all tie: lowest indices kept
+
+
+def test_identical_keys_different_values_diverge():
+    # rows 30 and 31 are kept rows (seen by every query) with equal keys
+    B, H, k0, m = 1, 1, 48, 16
+    k = synth.clustered_keys(10, B, H, k0 + m)
+    v = synth.planted_spectrum_values(11, B, H, k0 + m)
+    k[0, 0, 31] = k[0, 0, 30]
+    v[0, 0, 31] = synth.f32_to_bf16_bits(0.01 * synth.bf16_bits_to_f32(v[0, 0, 30]))
+    gpu, view, attn, lev, gaps = _run_block(B, H, 128, k[:, :, :k0], v[:, :, :k0], np.zeros((B, H, k0)),
+                                            k[:, :, k0:], v[:, :, k0:])
+    assert attn[0, 0, 30] == attn[0, 0, 31]
+    assert lev[0, 0, 30] > 100 * lev[0, 0, 31]
+
+
+def test_planted_geometry_class1_fills_the_budget_small():
+    B, H, S0, m = 2, 2, 3000, 128
+    p = synth.curdkv_planted(B, H, existing=S0, incoming=m, seed=5)
+    cum0 = np.zeros((B, H, S0))
+    gpu, view, attn, lev, gaps = _run_block(B, H, 256, p["k"][:, :, :S0], p["v"][:, :, :S0], cum0,
+                                            p["k"][:, :, S0:], p["v"][:, :, S0:], assert_lev=False)
+    gp = to_bits(view[2])
+    for b in range(B):
+        for h in range(H):
+            assert np.all(p["cls"][b, h, gp[b, h, 4:]] == 1)
+
+
+def test_planted_geometry_full_size_sampled_units():
+    # 8 x 8 heads, 16384 existing rows + a 512-token block, budget 2048, n_sink 4
+    B, H, S0, m = 8, 8, 16384, 512
+    p = synth.curdkv_planted(B, H, existing=S0, incoming=m)
+    cum0 = np.zeros((B, H, S0))
+    gpu, view, attn, lev, gaps = _run_block(B, H, 2048, p["k"][:, :, :S0], p["v"][:, :, :S0], cum0,
+                                            p["k"][:, :, S0:], p["v"][:, :, S0:], assert_lev=False,
+                                            units={(0, 0), (5, 3), (7, 7)})
+    gp = to_bits(view[2])
+    assert gp.shape == (B, H, 2048)
+    for b in range(B):
+        for h in range(H):
+            assert np.all(p["cls"][b, h, gp[b, h, 4:]] == 1), (b, h)
+
+
+def test_single_token_steps_after_prefill():
+    B, H = 1, 2
+    k_all = synth.clustered_keys(12, B, H, 140)
+    v_all = synth.planted_spectrum_values(13, B, H, 140)
+    ref = OracleCache("curdkv", B, H, budget=64, n_sink=4, rank_cap=RANK)
+    ref.update_and_fetch(k_all[:, :, :128], v_all[:, :, :128])
+    for t in range(128, 140):
+        # every step starts from the oracle's state
+        _run_block(B, H, 64, ref.k, ref.v, ref.score, k_all[:, :, t:t + 1], v_all[:, :, t:t + 1])
+        ref.update_and_fetch(k_all[:, :, t:t + 1], v_all[:, :, t:t + 1])
+
+
+def test_two_runs_are_bit_identical():
+    B, H, n = 2, 2, 700
+    k = synth.clustered_keys(14, B, H, n)
+    v = synth.planted_spectrum_values(15, B, H, n)
+    outs = []
+    for _ in range(2):
+        gpu = _gpu_cache(B, H, 128, max_block=n)
+        view = gpu.update_and_fetch(to_dev(k, torch), to_dev(v, torch))
+        gpu.sync()
+        outs.append([to_bits(t).copy() for t in view] + list(_gpu_scores(gpu, B, H)))
+    for a, b in zip(*outs):
+        assert a.tobytes() == b.tobytes()
