@@ -44,6 +44,7 @@ sys.path.insert(0, ROOT)
 from kv_cache_token_bf16_gb300 import synth  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 METRIC = "cache tokens evicted-and-compacted/sec per layer; achieved HBM GB/s vs roofline"
 UNIT = "tokens/s"
 
@@ -58,6 +59,8 @@ WORKLOADS = {
                    recent=128, dtype="bf16"),
     "long_context": dict(method="knorm", layers=1, batch=4, heads=8, block=8192, blocks=16, budget=4096, n_sink=4,
                          recent=0, dtype="bf16"),
+    "curdkv_planted": dict(method="curdkv", layers=1, batch=8, heads=8, existing=16384, incoming=512,
+                           budget=2048, n_sink=4, recent=0, rank_cap=16, dtype="bf16"),
     "knorm_single": dict(method="knorm", layers=1, batch=1, heads=1, seq=1024, budget=512, n_sink=4, recent=0,
                          dtype="fp32"),
 }
@@ -71,12 +74,14 @@ def _dist():
 
 
 def _peaks():
+    """Roofline denominators: the measured copy bandwidth and bf16 GEMM rate."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"])}, \
+            "measured (MEASURED_PEAKS.json: HBM copy bandwidth; bf16 GEMM burst)"
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
 
 
 def _source_hash(*names):
@@ -178,6 +183,7 @@ class StackRun:
         self.vp = [t.data_ptr() for t in self.v]
         self.tokens_per_step = L * w["batch"] * H * S
         self.calls_per_step = 1
+        self.rows_per_call = S
 
     def step(self):
         for h in self.handles:
@@ -228,6 +234,7 @@ class DecodeRun:
         self.i = 0
         self.tokens_per_step = B * H * (w["budget"] + 1)
         self.calls_per_step = 1
+        self.rows_per_call = w["budget"] + 1
 
     def step(self):
         s = self.i % self.w["steps"]
@@ -266,13 +273,27 @@ class LongContextRun:
             k, v = synth.long_context_block(blk, B, H, w["block"])
             self.k.append(torch.from_numpy(k.view(np.int16)).cuda().view(torch.bfloat16))
             self.v.append(torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16))
+        extra = {}
+        if w["method"] == "qfilters":
+            q = synth.long_context_queries(H)
+            qd = torch.from_numpy(q.view(np.int16)).cuda()
+            f = torch.empty((H, 128), dtype=torch.float32, device="cuda")
+            binding.evict_qfilters_calibrate(qd.data_ptr(), binding.EVICT_BF16, H, q.shape[1], 128, H,
+                                             f.data_ptr(), stream.cuda_stream)
+            extra = {"filters": f, "sign": 1}
+        if w["method"] == "curdkv":
+            extra = {"rank_cap": 16}
         self.cache = binding.EvictCache(w["method"], B, H, budget=w["budget"], n_sink=w["n_sink"],
-                                        recent=w["recent"], max_block=w["block"], stream=stream.cuda_stream)
+                                        recent=w["recent"], max_block=w["block"], stream=stream.cuda_stream, **extra)
         self.handle = self.cache.handle
         self.handles = [self.handle]
         per_bh = sum(min(blk * w["block"], w["budget"]) + w["block"] for blk in range(w["blocks"]))
+        kk = [min(blk * w["block"], w["budget"]) for blk in range(w["blocks"])]
+        m = w["block"]
+        self.logits = B * H * sum(m * k + m * (m + 1) // 2 for k in kk)
         self.tokens_per_step = B * H * per_bh
         self.calls_per_step = w["blocks"]
+        self.rows_per_call = per_bh / w["blocks"]
 
     def step(self):
         self.binding.evict_reset(self.handle)
@@ -301,6 +322,51 @@ class LongContextRun:
         return w["batch"] * w["heads"] * w["block"] * (128 * 2 + 4)
 
 
+class CurdkvPlantedRun:
+    """CurDKV planted geometry: a 16384-row cache (reloaded before every step,
+    outside the timed events) absorbs a 512-token block whose keys are the
+    proxy queries; budget 2048."""
+
+    def __init__(self, w, torch, binding, stream):
+        self.w, self.torch, self.binding = w, torch, binding
+        B, H, S0, m = w["batch"], w["heads"], w["existing"], w["incoming"]
+        p = synth.curdkv_planted(B, H, existing=S0, incoming=m)
+        dev = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.bfloat16)
+        self.k0, self.v0 = dev(p["k"][:, :, :S0]), dev(p["v"][:, :, :S0])
+        self.kn, self.vn = dev(p["k"][:, :, S0:]), dev(p["v"][:, :, S0:])
+        self.pos0 = torch.arange(S0, dtype=torch.int32, device="cuda").expand(B, H, S0).contiguous()
+        self.score0 = torch.zeros((B, H, S0), dtype=torch.float32, device="cuda")
+        self.cache = binding.EvictCache("curdkv", B, H, budget=w["budget"], n_sink=w["n_sink"], recent=w["recent"],
+                                        max_block=m, max_kept=S0, rank_cap=w["rank_cap"], stream=stream.cuda_stream)
+        self.handle = self.cache.handle
+        self.handles = [self.handle]
+        self.tokens_per_step = B * H * (S0 + m)
+        self.calls_per_step = 1
+        self.rows_per_call = S0 + m
+        self.logits = B * H * (m * S0 + m * (m + 1) // 2)
+
+    def reload(self):
+        self.binding.evict_set_state(self.handle, self.k0.data_ptr(), self.v0.data_ptr(), self.pos0.data_ptr(),
+                                     self.score0.data_ptr(), self.w["existing"], self.w["existing"])
+
+    def step(self):
+        self.binding.evict_update_and_fetch(self.handle, self.kn.data_ptr(), self.vn.data_ptr(), None,
+                                            self.w["incoming"])
+
+    def setup_e2e(self):
+        t = self.torch
+        self.kh = self.kn.view(t.int16).cpu().pin_memory()
+        self.vh = self.vn.view(t.int16).cpu().pin_memory()
+        self.out_h = t.empty((self.w["batch"] * self.w["heads"] * self.w["budget"],), dtype=t.int32).pin_memory()
+        self.h2d, self.d2h = 2 * self.kh.numel() * 2, self.out_h.numel() * 4
+
+    def step_e2e(self):
+        view = self.binding.evict_update_and_fetch_host(self.handle, self.kh.data_ptr(), self.vh.data_ptr(), None,
+                                                        self.w["incoming"])
+        pos = self.binding.view_tensors(view, self.w["batch"], self.w["heads"], "bf16")[2]
+        self.out_h.copy_(pos.reshape(-1), non_blocking=True)
+
+
 class KnormSingleRun:
     def __init__(self, w, torch, binding, stream):
         self.w, self.torch, self.binding = w, torch, binding
@@ -312,6 +378,7 @@ class KnormSingleRun:
         self.handles = [self.handle]
         self.tokens_per_step = w["seq"]
         self.calls_per_step = 1
+        self.rows_per_call = w["seq"]
 
     def step(self):
         self.binding.evict_reset(self.handle)
@@ -335,7 +402,7 @@ class KnormSingleRun:
 
 
 RUNS = {"qfilters_stack": StackRun, "decode": DecodeRun, "long_context": LongContextRun,
-        "knorm_single": KnormSingleRun}
+        "knorm_single": KnormSingleRun, "curdkv_planted": CurdkvPlantedRun}
 
 
 def run_ours(args):
@@ -368,16 +435,19 @@ def run_ours(args):
     for h in run.handles[:1]:
         binding.evict_set_profiling(h, True)
     launches0 = binding.evict_launch_count()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reload = getattr(run, "reload", None)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         barrier()
-        ev0.record(stream)
-        for _ in range(args.steps):
+        for a, b in evs:
+            if reload:
+                reload()               # restores the pre-existing cache; outside the timed events
+            a.record(stream)
             run.step()
-        ev1.record(stream)
+            b.record(stream)
         barrier()
     launches = binding.evict_launch_count() - launches0
-    ms = ev0.elapsed_time(ev1)
+    ms = sum(a.elapsed_time(b) for a, b in evs)
     ktimes = binding.evict_kernel_times(run.handles[0])
     binding.evict_set_profiling(run.handles[0], False)
     for h in run.handles:
@@ -394,40 +464,58 @@ def run_ours(args):
     for _ in range(min(args.warmup, 3)):
         run.step_e2e()
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    for a, b in e2e_evs:
+        if reload:
+            reload()
+        a.record(stream)
         run.step_e2e()
-    e1.record(stream)
+        b.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_evs) / args.steps
     if world > 1:
         t = torch.tensor([e2e_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
 
-    peak, peak_kind = _peaks()
-    alg_bytes = algorithmic_bytes(run, binding)
+    peaks, peak_kind = _peaks()
+    work = algorithmic_work(run, binding)
     kernels = {}
     tot = sum(t for _, t in ktimes.values())
     for k, (n, t) in ktimes.items():
+        sec = t / n / 1e3
         kernels[k] = {"launches": n, "avg_us": round(t / n * 1e3, 2), "share": round(t / tot, 4) if tot else None}
-        if k in alg_bytes:
-            kernels[k]["algorithmic_bytes_per_launch"] = alg_bytes[k]
-            kernels[k]["achieved_gbs"] = round(alg_bytes[k] / (t / n / 1e3) / 1e9, 1)
+        wk = work.get(k, {})
+        if "bytes" in wk:
+            kernels[k]["algorithmic_bytes_per_launch"] = wk["bytes"]
+            kernels[k]["achieved_gbs"] = round(wk["bytes"] / sec / 1e9, 1)
+        if "flops" in wk:
+            kernels[k]["algorithmic_flops_per_launch"] = wk["flops"]
+            kernels[k]["achieved_tflops"] = round(wk["flops"] / sec / 1e12, 2)
+        if "exps" in wk:
+            kernels[k]["exp2_per_s"] = round(wk["exps"] / sec, 1)
     roof = None
     if ktimes:
         top = max(ktimes, key=lambda k: ktimes[k][1])
         n_launch, tot_ms = ktimes[top]
         per_launch_ms = tot_ms / n_launch
-        alg = alg_bytes.get(top)
-        achieved = alg / (per_launch_ms / 1e3) / 1e9 if alg else None
-        roof = {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
-                "peak": peak, "peak_kind": peak_kind + " (HBM copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback", "unit": "GB/s",
-                "frac": round(achieved / peak, 4) if achieved else None,
-                "traffic": _ncu_traffic(top, args.workload), "algorithmic_bytes_per_launch": alg,
-                "avg_launch_us": round(per_launch_ms * 1e3, 2)}
+        wk = work.get(top, {})
+        if "bytes" in wk:
+            achieved = wk["bytes"] / (per_launch_ms / 1e3) / 1e9
+            roof = {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "algorithmic_bytes_per_launch": wk["bytes"]}
+        elif "flops" in wk and top in ("curdkv_lse", "curdkv_colsum"):
+            achieved = wk["flops"] / (per_launch_ms / 1e3) / 1e12
+            roof = {"kernel": top, "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "algorithmic_flops_per_launch": wk["flops"]}
+        else:
+            roof = {"kernel": top, "bound": "latency", "achieved": None, "peak": None, "unit": None, "frac": None}
+        roof["peak_kind"] = peak_kind
+        roof["traffic"] = _ncu_traffic(top, args.workload)
+        roof["avg_launch_us"] = round(per_launch_ms * 1e3, 2)
     cpu = cpu_baseline(args.workload) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     if rank == 0:
         line = {
@@ -455,9 +543,10 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def algorithmic_bytes(run, binding):
-    """Bytes each kernel must move per launch (one launch covers every layer of a call).
+def algorithmic_work(run, binding):
+    """Work each kernel must do per launch (one launch covers every layer of a call).
 
+    Bytes (HBM-bound kernels):
     score    : read each incoming key once, write its fp32 score.
     select   : read the n scores of every (b, h), write the budget-long source
                map, reset the chunk flags, write the 8-byte metadata.
@@ -466,23 +555,34 @@ def algorithmic_bytes(run, binding):
                row whose slot changes read and write K, V, position and score
                and read its map entry (4*D*e + 20 bytes). Rows counted from
                the last call (evict_compaction_rows).
+    curdkv_leverage : read every row's value once, its attention sum, and
+               read/write its score (D*2 + 12 bytes per row).
+    Flops / exponentials (CurDKV attention passes): 2*D per valid logit and
+    one exponential per valid logit; L = sum over (b, h) of m*k + m(m+1)/2.
+    curdkv_gram: 2*D*D flops per row (fp32 FMA on CUDA cores).
     """
     w = run.w
     e = 2 if w["dtype"] == "bf16" else 4
     units = w["layers"] * w["batch"] * w["heads"]
-    out = {}
-    m = w.get("seq", w.get("block", 1))
+    m = w.get("seq", w.get("block", w.get("incoming", 1)))
     if isinstance(run, DecodeRun):
         m = 1
-    out["score"] = units * m * (128 * e + 4)
+    n = run.rows_per_call
+    out = {"score": {"bytes": units * m * (128 * e + 4)}}
     old, new = 0, 0
     for h in run.handles:
         a, b = binding.evict_compaction_rows(h)
         old, new = old + a, new + b
-    out["compact"] = new * (4 * 128 * e + 16) + old * (4 * 128 * e + 20)
-    n = w["budget"] + m if not isinstance(run, StackRun) else m
+    out["compact"] = {"bytes": new * (4 * 128 * e + 16) + old * (4 * 128 * e + 20)}
     flag_stride = -(-w["budget"] // (32 if e == 2 else 16))
-    out["select"] = units * (4 * n + 4 * w["budget"] + 4 * flag_stride + 8)
+    out["select"] = {"bytes": int(units * (4 * n + 4 * w["budget"] + 4 * flag_stride + 8))}
+    logits = getattr(run, "logits", None)
+    if logits:
+        calls = run.calls_per_step
+        for k in ("curdkv_lse", "curdkv_colsum"):
+            out[k] = {"flops": 2 * 128 * logits / calls, "exps": logits / calls}
+        out["curdkv_gram"] = {"flops": units * n * 2 * 128 * 128}
+        out["curdkv_leverage"] = {"bytes": int(units * n * (128 * 2 + 12))}
     return out
 
 
@@ -526,19 +626,40 @@ def _oracle_sample(workload, budget_s=10.0):
                 break
         return tokens, time.perf_counter() - t0, f"{done} decode steps after the 2048-token prefill"
     if workload == "long_context":
-        c = OracleCache(w["method"], w["batch"], w["heads"], budget=w["budget"], n_sink=w["n_sink"],
-                        recent=w["recent"])
+        # one (b, h) unit followed through the stream (units are independent)
+        kw = {}
+        if w["method"] == "qfilters":
+            kw = {"filters": ocal.calibrate(synth.long_context_queries(w["heads"]), w["heads"])[:1]
+                  .astype(np.float32), "sign": 1}
+        c = OracleCache(w["method"], 1, 1, budget=w["budget"], n_sink=w["n_sink"], recent=w["recent"], **kw)
         for blk in range(w["blocks"]):
             k, v = synth.long_context_block(blk, w["batch"], w["heads"], w["block"])
             t1 = time.perf_counter()
             n = c.n_kept + w["block"]
-            c.update_and_fetch(k, v)
+            c.update_and_fetch(k[:1, :1], v[:1, :1])
             secs += time.perf_counter() - t1
-            tokens += w["batch"] * w["heads"] * n
+            tokens += n
             done += 1
             if secs > budget_s:
                 break
-        return tokens, secs, f"{done} of {w['blocks']} blocks"
+        return tokens, secs, f"{done} of {w['blocks']} blocks of one (b, h) unit"
+    if workload == "curdkv_planted":
+        S0, m = w["existing"], w["incoming"]
+        p = synth.curdkv_planted(w["batch"], w["heads"], existing=S0, incoming=m)
+        t0 = time.perf_counter()
+        for b in range(w["batch"]):
+            for h in range(w["heads"]):
+                c = OracleCache("curdkv", 1, 1, budget=w["budget"], n_sink=w["n_sink"], rank_cap=w["rank_cap"])
+                c.set_state(p["k"][b:b + 1, h:h + 1, :S0], p["v"][b:b + 1, h:h + 1, :S0],
+                            np.arange(S0, dtype=np.int32)[None, None], np.zeros((1, 1, S0)), S0)
+                t1 = time.perf_counter()
+                c.update_and_fetch(p["k"][b:b + 1, h:h + 1, S0:], p["v"][b:b + 1, h:h + 1, S0:])
+                secs += time.perf_counter() - t1
+                tokens += S0 + m
+                done += 1
+                if time.perf_counter() - t0 > budget_s:
+                    return tokens, secs, f"{done} of {w['batch'] * w['heads']} (b, h) units (one update each)"
+        return tokens, secs, f"{done} (b, h) units (one update each)"
     k, v = synth.knorm_single_sequence(w["seq"])
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < min(budget_s, 2.0):
@@ -588,9 +709,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qfilters_stack")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--method", choices=["knorm", "qfilters", "curdkv"], default=None,
+                    help="scorer for the long_context and decode workloads")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    if args.method:
+        if args.workload not in ("long_context", "decode") or (args.workload == "decode" and args.method == "curdkv"):
+            ap.error("--method applies to long_context (any scorer) and decode (knorm, qfilters)")
+        WORKLOADS[args.workload]["method"] = args.method
     if args.impl == "reference":
         run_reference(args)
     else:
