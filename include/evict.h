@@ -174,8 +174,8 @@ int evict_get_view(const evict_handle* h, evict_view* out);
  * and the call returns without synchronising.
  * Intermediate data lives in one fixed 8 MiB device array inside the library
  * (held by every GPU that loads it until process exit). A call needs
- * B*H*(4n + 4*budget + 8 + 4*ceil(budget/chunk)) bytes of it plus small
- * rounding (chunk = 32 rows for bf16, 16 for fp32); larger calls return
+ * B*H*(4n + 4*budget + 8 + 4*(ceil(budget/chunk) + 1)) bytes of it plus small
+ * rounding (chunk = 64 rows for bf16, 32 for fp32); larger calls return
  * EVICT_ELIMIT. The first call on a device looks up the array's address with
  * that device current — make it before any stream capture. All calls on a
  * device share the array, so calls that overlap on the GPU race.

@@ -39,8 +39,8 @@ struct evict_handle {
   evict_config cfg;
   int elem = 2;               // bytes per K/V element
   int cap = 0;                // storage rows per (b, h)
-  int chunk = 32;             // compaction chunk rows
-  int flag_stride = 0;        // compaction chunks per (b, h)
+  int chunk = 64;             // compaction chunk rows
+  int flag_stride = 0;        // compaction flag slots per (b, h): chunk flags + chunk counter
   int new_stride = 0;         // row stride of new_score (= max_block)
   cudaStream_t stream = nullptr;
 
@@ -55,7 +55,6 @@ struct evict_handle {
   int32_t* src_map = nullptr;
   int2* meta = nullptr;
   int* flags = nullptr;
-  int* ticket = nullptr;
   int* err = nullptr;
   void* k_stage = nullptr;
   void* v_stage = nullptr;

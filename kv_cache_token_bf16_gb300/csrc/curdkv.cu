@@ -62,8 +62,7 @@ constexpr int kAttnSmem = 2 * kTileBytes + 1024 + 1024;   // two tiles + alignme
 constexpr int kGramThreads = 256;
 constexpr int kGramRows = 1024;             // rows per Gram partial
 constexpr int kGramTileRows = 32;
-constexpr int kEigThreads = 512;
-constexpr int kStride = kHeadDim + 1;       // padded row stride of G in shared memory
+constexpr int kEigThreads = 1024;
 constexpr int kMbarSpin = 1 << 22;          // bounded MMA wait (well above a tile's time)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -346,20 +345,25 @@ __global__ void __launch_bounds__(kGramThreads) curdkv_gram_kernel(const __grid_
 }
 
 // ---------------------------------------------------------------------------
-// Top-r eigenvectors of G (symmetric, 128 x 128), one CTA per (b, h).
+// Top-r eigenvectors of G (symmetric, 128 x 128), one CTA of 512 threads per
+// (b, h). G is normalised by its trace and held in registers: kGroup threads
+// share a row, thread t owning row t/kGroup and the columns c = t%kGroup
+// (mod kGroup).
 // ---------------------------------------------------------------------------
+constexpr int kGroup = kEigThreads / kHeadDim; // threads per row
+constexpr int kEigPer = kHeadDim / kGroup;     // columns per thread
+
 struct EigSmem {
   double trace;
   double diag64[kHeadDim];
-  float a[kHeadDim * kStride];        // G, then the Householder vectors below the diagonal
-  float v[kHeadDim], pv[kHeadDim], w[kHeadDim];
+  float hv[kHeadDim - 2][kHeadDim];   // Householder vector of step j (zeros up to index j)
+  float x[2][kHeadDim], pv[2][kHeadDim];
+  float gram[kCurdkvMaxRank][kCurdkvMaxRank + 1];
   float d[kHeadDim], e[kHeadDim], e2[kHeadDim], beta[kHeadDim];
   float lam[kCurdkvMaxRank];
   float z[kCurdkvMaxRank][kHeadDim];  // eigenvectors (tridiagonal basis, then original)
-  float lu[16][5][kHeadDim];          // per-warp LU factors: diag, sup1, sup2, mult, pivot flag
-  float dots[kCurdkvMaxRank];
-  float scal, tnorm;
-  int n_active;
+  float lu[kCurdkvMaxRank][5][kHeadDim];  // per-vector LU factors: diag^-1, sup1, sup2, mult, pivot flag
+  float tnorm;
 };
 
 // Number of eigenvalues of the (normalised) tridiagonal T that are <= x.
@@ -368,8 +372,9 @@ __device__ __forceinline__ int sturm_count(const EigSmem& s, float x, float pivm
   float q = s.d[0] - x;
   if (fabsf(q) < pivmin) q = -pivmin;
   if (q <= 0.f) ++cnt;
+#pragma unroll 4
   for (int i = 1; i < kHeadDim; ++i) {
-    q = s.d[i] - s.e2[i - 1] / q - x;
+    q = s.d[i] - __fdividef(s.e2[i - 1], q) - x;
     if (fabsf(q) < pivmin) q = -pivmin;
     if (q <= 0.f) ++cnt;
   }
@@ -384,23 +389,33 @@ __device__ __forceinline__ float hash_unit(int i, int j) {
   return (float)(h & 0xFFFFu) * (1.f / 65536.f) - 0.5f;
 }
 
-__global__ void __launch_bounds__(kEigThreads) curdkv_eig_kernel(const __grid_constant__ CurdkvParams p) {
+__global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(16) unsigned char eig_raw[];
   EigSmem& s = *reinterpret_cast<EigSmem*>(eig_raw);
   const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int n = kHeadDim;
+  constexpr int kWarps = kEigThreads / 32;
   const int r = p.rank;
   float* evec_out = p.evec + (size_t)bh * kCurdkvMaxRank * n;
+  const int row = tid / kGroup, q4 = tid % kGroup;   // q4: this thread's column class
 
-  // G = sum of partials (fp64, fixed order), then fp32; E = trace in fp64
+  // G = sum of the partials in a fixed order: fp32, except the diagonal terms
+  // that form E = trace G (fp64; GB300's fp64 rate is low, so only those)
   const int splits_used = (p.n + kGramRows - 1) / kGramRows;
-  for (int el = tid; el < n * n; el += kEigThreads) {
-    double acc = 0.0;
-    const float* src = p.gram_part + (size_t)bh * p.splits * n * n + el;
-    for (int sp = 0; sp < splits_used; ++sp) acc += src[(size_t)sp * n * n];
-    const int row = el / n, col = el % n;
-    s.a[row * kStride + col] = (float)acc;
-    if (row == col) s.diag64[row] = acc;
+  const float* part = p.gram_part + (size_t)bh * p.splits * n * n + row * n + q4;
+  float a[kEigPer];
+#pragma unroll
+  for (int i = 0; i < kEigPer; ++i) a[i] = 0.f;
+  for (int sp = 0; sp < splits_used; ++sp) {        // branch-free so the loads overlap
+    const float* src = part + (size_t)sp * n * n;
+#pragma unroll
+    for (int i = 0; i < kEigPer; ++i) a[i] += src[kGroup * i];
+  }
+  if (row % kGroup == q4) {                          // this thread holds G[row][row]
+    const float* src = p.gram_part + (size_t)bh * p.splits * n * n + row * n + row;
+    double diag = 0.0;
+    for (int sp = 0; sp < splits_used; ++sp) diag += src[(size_t)sp * n * n];
+    s.diag64[row] = diag;
   }
   __syncthreads();
   if (tid == 0) {
@@ -414,79 +429,122 @@ __global__ void __launch_bounds__(kEigThreads) curdkv_eig_kernel(const __grid_co
     if (tid == 0) p.inv_e[bh] = 0.f;
     return;
   }
-  if (tid == 0) {
-    p.inv_e[bh] = (float)(1.0 / s.trace);
-    s.scal = (float)(1.0 / s.trace);          // normalise G: eigenvectors unchanged
+  if (tid == 0) p.inv_e[bh] = (float)(1.0 / s.trace);
+  {
+    const float sc = (float)(1.0 / s.trace);     // normalise: eigenvectors unchanged
+#pragma unroll
+    for (int i = 0; i < kEigPer; ++i) a[i] *= sc;
   }
-  __syncthreads();
-  for (int el = tid; el < n * kStride; el += kEigThreads) s.a[el] *= s.scal;
-  __syncthreads();
 
-  // --- Householder tridiagonalisation ---------------------------------------
+  // --- Householder tridiagonalisation (registers) ----------------------------
+  // a[i] holds column kGroup*(i + base) + q4; every kGroup steps the row
+  // shifts left by one (the finished columns drop out), so the column being
+  // reduced is always a[0], every register index is a compile-time constant
+  // and the loops stop at the last live column (a CTA-uniform bound).
+  // Step j works with x = column j below the diagonal, zero-filled up to
+  // index j in shared memory; the Householder vector v equals x except
+  // v[j+1] = x[j+1] + delta, which enters as one correction term. Each step
+  // has two barriers: every warp recomputes the step's scalars from the
+  // shared vectors (identical bits in every warp), and the vectors are
+  // double-buffered by step parity. Warps whose rows are all finished skip.
+  constexpr int kRowsPerWarp = 32 / kGroup;
+  int base = 0;
   for (int j = 0; j < n - 2; ++j) {
-    const int L = n - 1 - j;
+    float* xj = s.x[j & 1];
+    float* pj = s.pv[j & 1];
+    if (q4 == j % kGroup) {
+      xj[row] = row > j ? a[0] : 0.f;             // column j below the diagonal, zeros above
+      if (row == j) s.d[j] = a[0];                // diagonal element j
+    }
+    __syncthreads();
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ss = fmaf(xj[32 * k + lane], xj[32 * k + lane], ss);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float x0 = xj[j + 1];
+    const float tail = ss - x0 * x0;
+    float beta = 0.f, alpha = x0, delta = 0.f;
+    if (tail > 0.f) {
+      const float sigma = sqrtf(ss);
+      alpha = x0 >= 0.f ? -sigma : sigma;
+      delta = -alpha;                             // v[j+1] = x0 - alpha
+      beta = 1.f / (sigma * (sigma + fabsf(x0)));
+    }
     if (warp == 0) {
-      float ss = 0.f;
-      for (int ii = lane; ii < L; ii += 32) {
-        const float x = s.a[(j + 1 + ii) * kStride + j];
-        s.v[ii] = x;
-        ss += x * x;
-      }
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      for (int k = 0; k < 4; ++k) {
+        const int c = 32 * k + lane;
+        const float xv = xj[c];
+        s.hv[j][c] = beta == 0.f ? 0.f : (c == j + 1 ? xv + delta : xv);
+      }
       if (lane == 0) {
-        const float x0 = s.v[0];
-        const float tail = ss - x0 * x0;
-        if (!(tail > 0.f)) {                         // already tridiagonal in this column
-          s.beta[j] = 0.f;
-          s.e[j] = x0;
-        } else {
-          const float sigma = sqrtf(ss);
-          const float alpha = x0 >= 0.f ? -sigma : sigma;
-          s.v[0] = x0 - alpha;
-          s.beta[j] = 1.f / (sigma * (sigma + fabsf(x0)));
-          s.e[j] = alpha;
-        }
-        s.d[j] = s.a[j * kStride + j];
+        s.beta[j] = beta;
+        s.e[j] = alpha;
       }
     }
-    __syncthreads();
-    const float beta = s.beta[j];
+    const bool live_rows = warp * kRowsPerWarp + kRowsPerWarp - 1 > j;   // some row of this warp is > j
+    // index of column j+1 in this thread's registers, if this thread owns it
+    const bool owns_next = q4 == (j + 1) % kGroup;
+    const int next_idx = (j + 1) / kGroup - base;      // 0 or 1
     if (beta != 0.f) {
-      // p = beta * A_sub v, 4 threads per row
-      const int ii = tid >> 2, q = tid & 3;
+      // p = beta * A v = beta * (A x + A[:, j+1] * delta)
       float acc = 0.f;
-      if (ii < L) {
-        const float* row = s.a + (j + 1 + ii) * kStride + (j + 1);
-        for (int cc = q; cc < L; cc += 4) acc = fmaf(row[cc], s.v[cc], acc);
-      }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (ii < L && q == 0) s.pv[ii] = beta * acc;
-      __syncthreads();
-      if (warp == 0) {
-        float dot = 0.f;
-        for (int x = lane; x < L; x += 32) dot = fmaf(s.v[x], s.pv[x], dot);
+      if (live_rows) {
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        const float K = 0.5f * beta * dot;
-        for (int x = lane; x < L; x += 32) s.w[x] = s.pv[x] - K * s.v[x];
+        for (int i = 0; i < kEigPer; ++i) {
+          if (i + base >= kEigPer) break;
+          const float xc = xj[kGroup * (i + base) + q4];
+          if (i & 1) acc1 = fmaf(a[i], xc, acc1); else acc0 = fmaf(a[i], xc, acc0);
+        }
+        acc = acc0 + acc1;
+        if (owns_next) acc = fmaf(next_idx == 0 ? a[0] : a[1], delta, acc);
+#pragma unroll
+        for (int o = 1; o < kGroup; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       }
+      if (q4 == 0) pj[row] = row > j ? beta * acc : 0.f;
       __syncthreads();
-      if (ii < L) {
-        float* row = s.a + (j + 1 + ii) * kStride + (j + 1);
-        const float vi = s.v[ii], wi = s.w[ii];
-        for (int cc = q; cc < L; cc += 4) row[cc] -= vi * s.w[cc] + wi * s.v[cc];
+      // K = beta/2 * v.p, recomputed by every warp (p is zero up to index j)
+      float dot = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dot = fmaf(xj[32 * k + lane], pj[32 * k + lane], dot);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      dot = fmaf(delta, pj[j + 1], dot);
+      const float K = 0.5f * beta * dot;
+      if (live_rows) {
+        // A -= v w^T + w v^T, w = p - K v; computed with x for v, then the
+        // column j+1 term corrected by delta * (w_r - K v_r)
+        const float vr = row > j ? xj[row] + (row == j + 1 ? delta : 0.f) : 0.f;
+        const float wr = pj[row] - K * vr;
+#pragma unroll
+        for (int i = 0; i < kEigPer; ++i) {
+          if (i + base >= kEigPer) break;
+          const int c = kGroup * (i + base) + q4;
+          const float xc = xj[c];
+          a[i] -= vr * fmaf(-K, xc, pj[c]) + wr * xc;
+        }
+        if (owns_next) {
+          const float corr = delta * (wr - K * vr);
+          if (next_idx == 0) a[0] -= corr; else a[1] -= corr;
+        }
       }
-      // keep the Householder vector in column j (below the diagonal)
-      if (tid < L) s.a[(j + 1 + tid) * kStride + j] = s.v[tid];
     }
-    __syncthreads();
+    if (j % kGroup == kGroup - 1) {
+#pragma unroll
+      for (int i = 0; i < kEigPer - 1; ++i) a[i] = a[i + 1];
+      a[kEigPer - 1] = 0.f;
+      ++base;
+    }
   }
+  // last 2 x 2 block: after (n-2)/kGroup shifts a[0] holds column n-2-(n-2)%kGroup + q4
+  static_assert((kHeadDim - 2) % kGroup + 1 < kGroup, "columns n-2 and n-1 share a[0]");
+  if (row == n - 2 && q4 == (n - 2) % kGroup) s.d[n - 2] = a[0];
+  if (row == n - 1 && q4 == (n - 2) % kGroup) s.e[n - 2] = a[0];
+  if (row == n - 1 && q4 == (n - 1) % kGroup) s.d[n - 1] = a[0];
+  __syncthreads();
   if (tid == 0) {
-    s.d[n - 2] = s.a[(n - 2) * kStride + (n - 2)];
-    s.d[n - 1] = s.a[(n - 1) * kStride + (n - 1)];
-    s.e[n - 2] = s.a[(n - 1) * kStride + (n - 2)];
     s.e[n - 1] = 0.f;
     float tn = 0.f;
     for (int i = 0; i < n; ++i) {
@@ -502,13 +560,13 @@ __global__ void __launch_bounds__(kEigThreads) curdkv_eig_kernel(const __grid_co
   // --- top r eigenvalues by multisection (one warp per eigenvalue) ----------
   const float tnorm = s.tnorm;
   const float pivmin = FLT_MIN * 1e4f;
-  for (int jj = warp; jj < r; jj += kEigThreads / 32) {
+  for (int jj = warp; jj < r; jj += kWarps) {
     const int target = n - 1 - jj;                   // ascending index
     float lo = -tnorm * 1.01f - pivmin, hi = tnorm * 1.01f + pivmin;
     for (int round = 0; round < 8; ++round) {
       const float step = (hi - lo) / 33.f;
-      const float x = lo + step * (float)(lane + 1);
-      const int cnt = sturm_count(s, x, pivmin);
+      const float xv = lo + step * (float)(lane + 1);
+      const int cnt = sturm_count(s, xv, pivmin);
       const unsigned above = __ballot_sync(0xffffffffu, cnt >= target + 1);
       const int first = above ? __ffs(above) - 1 : 32;
       const float nlo = first == 0 ? lo : lo + step * (float)first;
@@ -523,39 +581,40 @@ __global__ void __launch_bounds__(kEigThreads) curdkv_eig_kernel(const __grid_co
 
   // --- inverse iteration (lane 0 of one warp per eigenvalue) -----------------
   const float guard = FLT_EPSILON * tnorm;
-  for (int jj = warp; jj < r; jj += kEigThreads / 32) {
-    float* dg = s.lu[warp][0];
-    float* u1 = s.lu[warp][1];
-    float* u2 = s.lu[warp][2];
-    float* ml = s.lu[warp][3];
-    float* pf = s.lu[warp][4];
+  for (int jj = warp; jj < r; jj += kWarps) {
+    float* rd = s.lu[jj][0];
+    float* u1 = s.lu[jj][1];
+    float* u2 = s.lu[jj][2];
+    float* ml = s.lu[jj][3];
+    float* pf = s.lu[jj][4];
     float* zz = s.z[jj];
     for (int i = lane; i < n; i += 32) zz[i] = hash_unit(i, jj) + 0.75f;
     __syncwarp();
     if (lane == 0) {
       const float lam = s.lam[jj];
-      // LU with partial pivoting of T - lam I (rows: sub e[i-1], diag d[i]-lam, super e[i])
+      // LU with partial pivoting of T - lam I (rows: sub e[i-1], diag d[i]-lam, super e[i]);
+      // rd holds the reciprocals of U's (guarded) diagonal
       float cd = s.d[0] - lam, cs = s.e[0];
       for (int i = 0; i < n - 1; ++i) {
         const float sub = s.e[i], nd = s.d[i + 1] - lam, ns = s.e[i + 1];
         if (fabsf(cd) >= fabsf(sub)) {
           if (fabsf(cd) < guard) cd = cd < 0.f ? -guard : guard;
-          const float l = sub / cd;
-          dg[i] = cd; u1[i] = cs; u2[i] = 0.f; ml[i] = l; pf[i] = 0.f;
+          const float inv = 1.f / cd;
+          const float l = sub * inv;
+          rd[i] = inv; u1[i] = cs; u2[i] = 0.f; ml[i] = l; pf[i] = 0.f;
           cd = nd - l * cs;
           cs = ns;
         } else {
           const float l = cd / sub;
-          dg[i] = fabsf(sub) < guard ? (sub < 0.f ? -guard : guard) : sub;
-          u1[i] = nd; u2[i] = ns; ml[i] = l; pf[i] = 1.f;
+          const float dg = fabsf(sub) < guard ? (sub < 0.f ? -guard : guard) : sub;
+          rd[i] = 1.f / dg; u1[i] = nd; u2[i] = ns; ml[i] = l; pf[i] = 1.f;
           cd = cs - l * nd;
           cs = -l * ns;
         }
       }
       if (fabsf(cd) < guard) cd = cd < 0.f ? -guard : guard;
-      dg[n - 1] = cd; u1[n - 1] = 0.f; u2[n - 1] = 0.f;
-      for (int it = 0; it < 3; ++it) {
-        // forward: apply the row swaps and multipliers to the right-hand side
+      rd[n - 1] = 1.f / cd; u1[n - 1] = 0.f; u2[n - 1] = 0.f;
+      for (int it = 0; it < 2; ++it) {
         for (int i = 0; i < n - 1; ++i) {
           if (pf[i] != 0.f) {
             const float t = zz[i];
@@ -565,12 +624,13 @@ __global__ void __launch_bounds__(kEigThreads) curdkv_eig_kernel(const __grid_co
             zz[i + 1] -= ml[i] * zz[i];
           }
         }
-        // back substitution with the three-diagonal U
-        zz[n - 1] = zz[n - 1] / dg[n - 1];
-        zz[n - 2] = (zz[n - 2] - u1[n - 2] * zz[n - 1]) / dg[n - 2];
-        for (int i = n - 3; i >= 0; --i) zz[i] = (zz[i] - u1[i] * zz[i + 1] - u2[i] * zz[i + 2]) / dg[i];
-        float mx = 0.f;
-        for (int i = 0; i < n; ++i) mx = fmaxf(mx, fabsf(zz[i]));
+        zz[n - 1] = zz[n - 1] * rd[n - 1];
+        zz[n - 2] = (zz[n - 2] - u1[n - 2] * zz[n - 1]) * rd[n - 2];
+        float mx = fmaxf(fabsf(zz[n - 1]), fabsf(zz[n - 2]));
+        for (int i = n - 3; i >= 0; --i) {
+          zz[i] = (zz[i] - u1[i] * zz[i + 1] - u2[i] * zz[i + 2]) * rd[i];
+          mx = fmaxf(mx, fabsf(zz[i]));
+        }
         const float inv = mx > 0.f ? 1.f / mx : 0.f;
         for (int i = 0; i < n; ++i) zz[i] *= inv;
       }
@@ -579,50 +639,72 @@ __global__ void __launch_bounds__(kEigThreads) curdkv_eig_kernel(const __grid_co
   }
   __syncthreads();
 
-  // --- orthonormalise the r vectors (modified Gram-Schmidt, two passes) -----
+  // --- orthonormalise the r vectors: Cholesky-QR, two passes ---------------
+  // M = Z Z^T = L L^T, Z <- L^{-1} Z. A non-positive pivot (a dependent
+  // vector) drops that vector.
   for (int pass = 0; pass < 2; ++pass) {
-    for (int jj = 0; jj < r; ++jj) {
-      // dots with the previous vectors (one warp each)
-      for (int kk = warp; kk < jj; kk += kEigThreads / 32) {
-        float dot = 0.f;
-        for (int i = lane; i < n; i += 32) dot = fmaf(s.z[kk][i], s.z[jj][i], dot);
+    for (int pr = warp; pr < r * r; pr += kWarps) {
+      const int ia = pr / r, ib = pr % r;
+      if (ib > ia) continue;
+      float dot = 0.f;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (lane == 0) s.dots[kk] = dot;
-      }
-      __syncthreads();
-      if (tid < n) {
-        float x = s.z[jj][tid];
-        for (int kk = 0; kk < jj; ++kk) x -= s.dots[kk] * s.z[kk][tid];
-        s.z[jj][tid] = x;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        float ss = 0.f;
-        for (int i = lane; i < n; i += 32) ss += s.z[jj][i] * s.z[jj][i];
+      for (int k = 0; k < 4; ++k) dot = fmaf(s.z[ia][32 * k + lane], s.z[ib][32 * k + lane], dot);
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
-        for (int i = lane; i < n; i += 32) s.z[jj][i] *= inv;
-      }
-      __syncthreads();
+      for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      if (lane == 0) s.gram[ia][ib] = dot;
     }
+    __syncthreads();
+    if (warp == 0) {                                   // in-place lower Cholesky factor, lane = row
+      for (int k = 0; k < r; ++k) {
+        // row k's entries left of the diagonal are final: finish column k
+        float dkk = 0.f;
+        if (lane == k) {
+          float acc = s.gram[k][k];
+          for (int m = 0; m < k; ++m) acc -= s.gram[k][m] * s.gram[k][m];
+          dkk = acc > 1e-20f ? sqrtf(acc) : 0.f;
+          s.gram[k][k] = dkk;
+        }
+        dkk = __shfl_sync(0xffffffffu, dkk, k);
+        if (lane > k && lane < r) {
+          float acc = s.gram[lane][k];
+          for (int m = 0; m < k; ++m) acc -= s.gram[lane][m] * s.gram[k][m];
+          s.gram[lane][k] = dkk > 0.f ? acc / dkk : 0.f;
+        }
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+    if (tid < n) {                                     // forward substitution in place, one column per thread
+      for (int ia = 0; ia < r; ++ia) {
+        float acc = s.z[ia][tid];
+        for (int ib = 0; ib < ia; ++ib) acc -= s.gram[ia][ib] * s.z[ib][tid];
+        s.z[ia][tid] = s.gram[ia][ia] > 0.f ? acc / s.gram[ia][ia] : 0.f;
+      }
+    }
+    __syncthreads();
   }
 
   // --- back-transform: y = H_0 H_1 ... H_{n-3} z  (one warp per vector) -----
-  for (int jj = warp; jj < r; jj += kEigThreads / 32) {
+  for (int jj = warp; jj < r; jj += kWarps) {
     float* y = s.z[jj];
+    float yl[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) yl[c] = y[lane + 32 * c];
     for (int j = n - 3; j >= 0; --j) {
       const float beta = s.beta[j];
       if (beta == 0.f) continue;
+      const float* hv = s.hv[j];
       float dot = 0.f;
-      for (int ii = lane; ii < n - 1 - j; ii += 32) dot = fmaf(s.a[(j + 1 + ii) * kStride + j], y[j + 1 + ii], dot);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) dot = fmaf(hv[lane + 32 * c], yl[c], dot);
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
       const float f = beta * dot;
-      for (int ii = lane; ii < n - 1 - j; ii += 32) y[j + 1 + ii] -= f * s.a[(j + 1 + ii) * kStride + j];
-      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) yl[c] -= f * hv[lane + 32 * c];
     }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) y[lane + 32 * c] = yl[c];
   }
   __syncthreads();
   for (int el = tid; el < kCurdkvMaxRank * n; el += kEigThreads) {

@@ -101,7 +101,6 @@ size_t arena_layout(evict_handle* h, char* base) {
   h->src_map = cv.take<int32_t>(bh * h->cap * 4);
   h->meta = cv.take<int2>(bh * sizeof(int2));
   h->flags = cv.take<int>(bh * h->flag_stride * 4);
-  h->ticket = cv.take<int>(4);
   h->err = cv.take<int>(4);
   h->k_stage = cv.take<void>(bh * c.max_block * kHeadDim * e);
   h->v_stage = cv.take<void>(bh * c.max_block * kHeadDim * e);
@@ -166,7 +165,6 @@ GroupParams make_group_params(const evict_handle* h, int m, int n_layers) {
   P.s.sign = (float)(c.method == EVICT_QFILTERS ? c.sign : 1);
   P.s.method = c.method;
   P.s.offset = h->offset;
-  P.ticket = h->ticket;
   P.err = h->err;
   return P;
 }
@@ -266,7 +264,7 @@ int evict_init(const evict_config* cfg, evict_handle** out) {
   h->cap = std::max(cfg->budget, cfg->max_kept);
   h->new_stride = cfg->max_block;
   h->chunk = compact_chunk_rows(h->elem);
-  h->flag_stride = (h->cap + h->chunk - 1) / h->chunk;
+  h->flag_stride = compact_flag_slots(h->cap, h->elem);
   h->stream = static_cast<cudaStream_t>(cfg->stream);
   const size_t bytes = arena_layout(h, nullptr);
   cudaError_t e = cudaMalloc(&h->arena, bytes);

@@ -9,6 +9,8 @@ namespace evict {
 
 // Rows per compaction chunk for an element size of 2 (bf16) or 4 (fp32) bytes.
 int compact_chunk_rows(int dtype_bytes);
+// Flag slots per (b, h) for caches of `rows` rows: chunk flags plus a chunk counter.
+int compact_flag_slots(int rows, int dtype_bytes);
 
 cudaError_t launch_score(const GroupParams& P, int dtype_bytes, cudaStream_t st);
 cudaError_t launch_append(const GroupParams& P, int dtype_bytes, cudaStream_t st);

@@ -92,8 +92,7 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
 
   const int elem = c.dtype == EVICT_BF16 ? 2 : 4;
   const size_t bh = (size_t)c.batch * c.n_kv_heads;
-  const int chunk = compact_chunk_rows(elem);
-  const int flag_stride = (c.budget + chunk - 1) / chunk;
+  const int flag_stride = compact_flag_slots(c.budget, elem);
   const size_t off_src = round256(bh * n * sizeof(float));
   const size_t off_meta = off_src + round256(bh * c.budget * sizeof(int32_t));
   const size_t off_flags = off_meta + round256(bh * sizeof(int2));
@@ -108,8 +107,9 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
   if (rc) return rc;
   char* s = static_cast<char*>(base);
   cudaStream_t st = static_cast<cudaStream_t>(c.stream);
-  // The ticket counter and the error word must start at zero; everything else
-  // in the scratch is written before it is read within this call.
+  // The error word must start at zero; everything else in the scratch is
+  // written before it is read within this call (the select kernel zeroes the
+  // compaction flags and counters).
   cudaError_t e = cudaMemsetAsync(s + off_words, 0, 256, st);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counters");
 
@@ -130,8 +130,7 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
   P.s.sign = (float)(c.method == EVICT_QFILTERS ? c.sign : 1);
   P.s.method = c.method;
   P.s.offset = 0;
-  P.ticket = reinterpret_cast<int*>(s + off_words);
-  P.err = reinterpret_cast<int*>(s + off_words + sizeof(int));
+  P.err = reinterpret_cast<int*>(s + off_words);
   LayerPtrs& L = P.L[0];
   L.k_in = k;
   L.v_in = v;

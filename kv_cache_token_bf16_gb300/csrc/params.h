@@ -24,7 +24,7 @@ struct LayerPtrs {
   float* new_score;        // [B, H, new_stride] scores of incoming rows
   int32_t* src_map;        // [B, H, cap] source row of each kept destination
   int2* meta;              // [B, H] {first moved destination, old survivors}
-  int* flags;              // [B, H, flag_stride] read-done flags of compaction chunks
+  int* flags;              // [B, H, flag_stride] compaction read-done flags, then the chunk counter
 };
 
 // Sizes common to every layer of a grouped update.
@@ -36,7 +36,7 @@ struct Shape {
   int budget;
   int n_sink, recent;
   int new_stride;          // row stride of new_score (max_block)
-  int flag_stride;         // chunks per (b, h)
+  int flag_stride;         // flag slots per (b, h): one per chunk + the chunk counter
   int n_layers;
   int keep_low;            // KNorm keep-low: priority = -score
   float sign;              // Q-Filters sign
@@ -46,7 +46,6 @@ struct Shape {
 
 struct GroupParams {
   Shape s;
-  int* ticket;             // compaction ticket counter (returns to 0 after each launch)
   int* err;                // device error word
   int total_ctas;          // compaction grid size
   LayerPtrs L[kMaxGroup];
