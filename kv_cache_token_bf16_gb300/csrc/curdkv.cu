@@ -20,12 +20,13 @@
 //                          (tcgen05 MMA, 128 queries x 128 keys per step, fp32 in TMEM)
 //   curdkv_colsum_kernel   pass 2: per key, sum over queries of 2^(logit*c - lse)
 //                          (tcgen05 MMA, 128 keys x 128 queries per step)
-//   curdkv_gram_kernel     partial G over a slice of rows (fp32 FMA)
+//   curdkv_gram_kernel     partial G over a slice of rows (tcgen05, split bf16)
 //   curdkv_eig_kernel      sum of partials (fp64), Householder tridiagonalisation,
 //                          multisection bisection for the top r eigenvalues,
 //                          inverse iteration, orthonormalisation, back-transform
 //   curdkv_leverage_kernel l_i and the cumulative-score update
 //   curdkv_append_kernel   copy of the block when the cache stays within budget
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -59,9 +60,7 @@ constexpr int kTile = 128;                  // rows of a query or key tile
 constexpr int kAttnThreads = 128;           // 4 warps: one TMEM lane per thread
 constexpr int kTileBytes = kTile * kHeadDim * 2;
 constexpr int kAttnSmem = 2 * kTileBytes + 1024 + 1024;   // two tiles + alignment + small arrays
-constexpr int kGramThreads = 256;
-constexpr int kGramRows = 1024;             // rows per Gram partial
-constexpr int kGramTileRows = 32;
+constexpr int kGramRows = 2048;             // rows per Gram partial
 constexpr int kEigThreads = 1024;
 constexpr int kMbarSpin = 1 << 22;          // bounded MMA wait (well above a tile's time)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -289,59 +288,159 @@ __global__ void __launch_bounds__(kAttnThreads) curdkv_colsum_kernel(const __gri
 }
 
 // ---------------------------------------------------------------------------
-// Partial Gram of the weighted values over rows [split * 1024, ...).
-// grid = (splits, B*H), block = 256; thread owns an 8 x 8 block of G.
+// Partial Gram of the weighted values on the tensor cores:
+//   G_part = sum over the split's rows i of a_i^2 v_i v_i^T
+//          = V^T (a^2 V)_hi + V^T (a^2 V)_lo,
+// V exact in bf16 and a_i^2 v_i split into two bf16 terms (hi + lo carries
+// ~16 significant bits; the dropped lo*lo-free remainder is below 2^-17 of
+// each term). The MMA contracts over tokens, so each 128-token tile is
+// transposed on the way into shared memory: a thread loads 8 tokens x 8
+// features (eight 16-byte rows) and rearranges them with byte permutes into
+// 8 features x 8 tokens. grid = (ceil(n / 2048), B*H), block = 128; the next
+// tile's loads overlap the running MMAs.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kGramThreads) curdkv_gram_kernel(const __grid_constant__ CurdkvParams p) {
-  __shared__ float tile[kGramTileRows][kHeadDim];
-  const int split = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
-  const int i0 = (tid >> 4) * 8, j0 = (tid & 15) * 8;
-  float acc[8][8];
+constexpr int kGramTcSmem = 3 * kTileBytes + 1024;
+
+// 8 x 8 transpose of bf16 values: in[t] holds 8 features of token t, out[f]
+// holds 8 tokens of feature f.
+__device__ __forceinline__ void transpose8x8(const uint4 (&in)[8], uint4 (&out)[8]) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(in);   // w[4*t + k]: features 2k, 2k+1 of token t
 #pragma unroll
-  for (int a = 0; a < 8; ++a)
-#pragma unroll
-    for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+  for (int f = 0; f < 8; ++f) {
+    const uint32_t sel = (f & 1) ? 0x7632u : 0x5410u;
+    const int k = f >> 1;
+    out[f].x = __byte_perm(w[4 * 0 + k], w[4 * 1 + k], sel);
+    out[f].y = __byte_perm(w[4 * 2 + k], w[4 * 3 + k], sel);
+    out[f].z = __byte_perm(w[4 * 4 + k], w[4 * 5 + k], sel);
+    out[f].w = __byte_perm(w[4 * 6 + k], w[4 * 7 + k], sel);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo_elem, hi_elem);   // .x (low half) = lo_elem
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__global__ void __launch_bounds__(kAttnThreads) curdkv_gram_kernel(const __grid_constant__ CurdkvParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_fail;
+  const int split = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t a_tile = tc::smem_u32(smem), bhi_tile = a_tile + kTileBytes, blo_tile = bhi_tile + kTileBytes;
   const int r_begin = split * kGramRows, r_end = min(p.n, r_begin + kGramRows);
   const float* attn = p.attn + (size_t)bh * p.rows;
-  for (int r0 = r_begin; r0 < r_end; r0 += kGramTileRows) {
-    for (int e = tid; e < kGramTileRows * 16; e += kGramThreads) {
-      const int rr = e >> 4, j = e & 15;
-      const int row = r0 + rr;
-      float x[8];
-      if (row < r_end) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(value_row(p, bh, row) + j * 16);
-        bf16x8_to_f32(raw, x);
-        const float a = attn[row];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] *= a;
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) tile[rr][j * 8 + q] = x[q];
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int rr = 0; rr < kGramTileRows; ++rr) {
-      float a[8], b[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        a[x] = tile[rr][i0 + x];
-        b[x] = tile[rr][j0 + x];
-      }
-#pragma unroll
-      for (int x = 0; x < 8; ++x)
-#pragma unroll
-        for (int y = 0; y < 8; ++y) acc[x][y] = fmaf(a[x], b[y], acc[x][y]);
-    }
-    __syncthreads();
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    s_fail = 0;
   }
-  float* out = p.gram_part + ((size_t)bh * p.splits + split) * kHeadDim * kHeadDim;
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kTile);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  // thread -> two 8x8 blocks of the tile: token block tb, feature blocks fb and fb + 8
+  const int tb = tid & 15, fb0 = tid >> 4;
+  uint4 raw[2][8];
+  float asq[8];
+  auto load_tile = [&](int t0) {
 #pragma unroll
-  for (int x = 0; x < 8; ++x)
+    for (int t = 0; t < 8; ++t) {
+      const int row = t0 + 8 * tb + t;
+      const bool ok = row < r_end;
+      const uint4* src = reinterpret_cast<const uint4*>(value_row(p, bh, ok ? row : r_begin));
+      raw[0][t] = ok ? __ldg(src + fb0) : make_uint4(0, 0, 0, 0);
+      raw[1][t] = ok ? __ldg(src + fb0 + 8) : make_uint4(0, 0, 0, 0);
+      const float a = ok ? attn[row] : 0.f;
+      asq[t] = a * a;
+    }
+  };
+  uint32_t parity = 0;
+  int pending = 0;                                          // commits not yet waited for
+  load_tile(r_begin);
+  for (int t0 = r_begin; t0 < r_end; t0 += kTile) {
+    if (pending) {                                          // smem tiles are free once the last MMAs finished
+      if (!wait_mma(&bar, parity, p.err)) s_fail = 1;
+      else pending = 0;
+      parity ^= 1u;
+      tc::fence_after_sync();
+    }
 #pragma unroll
-    for (int y = 0; y < 8; ++y) out[(i0 + x) * kHeadDim + j0 + y] = acc[x][y];
+    for (int h = 0; h < 2; ++h) {
+      const int fb = fb0 + 8 * h;
+      uint4 tr[8];
+      transpose8x8(raw[h], tr);
+#pragma unroll
+      for (int f = 0; f < 8; ++f)
+        *reinterpret_cast<uint4*>(smem + tc::sw128_offset(8 * fb + f, tb, kTile)) = tr[f];
+      uint4 hi[8], lo[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        float x[8];
+        bf16x8_to_f32(raw[h][t], x);
+        float y[8], yh[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) y[q] = x[q] * asq[t];
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hw[q] = pack_bf16x2(y[2 * q], y[2 * q + 1]);
+          yh[2 * q] = __uint_as_float(hw[q] << 16);
+          yh[2 * q + 1] = __uint_as_float(hw[q] & 0xffff0000u);
+          lw[q] = pack_bf16x2(y[2 * q] - yh[2 * q], y[2 * q + 1] - yh[2 * q + 1]);
+        }
+        hi[t] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        lo[t] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      transpose8x8(hi, tr);
+#pragma unroll
+      for (int f = 0; f < 8; ++f)
+        *reinterpret_cast<uint4*>(smem + kTileBytes + tc::sw128_offset(8 * fb + f, tb, kTile)) = tr[f];
+      transpose8x8(lo, tr);
+#pragma unroll
+      for (int f = 0; f < 8; ++f)
+        *reinterpret_cast<uint4*>(smem + 2 * kTileBytes + tc::sw128_offset(8 * fb + f, tb, kTile)) = tr[f];
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (s_fail) break;
+    if (tid == 0) {
+      tc::fence_after_sync();
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTile, kTile);
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        const uint32_t off = (uint32_t)((st >> 2) * kTile * 128 + (st & 3) * 32);
+        const uint64_t ad = tc::sw128_desc(a_tile + off);
+        tc::mma_bf16(tmem, ad, tc::sw128_desc(bhi_tile + off), idesc, (t0 > r_begin || st > 0) ? 1u : 0u);
+        tc::mma_bf16(tmem, ad, tc::sw128_desc(blo_tile + off), idesc, 1u);
+      }
+      tc::mma_commit(&bar);
+    }
+    pending = 1;
+    if (t0 + kTile < r_end) load_tile(t0 + kTile);          // overlaps with the MMAs
+  }
+  // the last commit (also on a failure path, so no MMA is in flight at dealloc)
+  if (pending && !wait_mma(&bar, parity, p.err)) s_fail = 1;
+  __syncthreads();
+  tc::fence_after_sync();
+  if (!s_fail) {
+    float* out = p.gram_part + ((size_t)bh * p.splits + split) * kHeadDim * kHeadDim + (size_t)tid * kHeadDim;
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+    for (int c0 = 0; c0 < kTile; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(trow + c0, v);
+#pragma unroll
+      for (int c = 0; c < 32; c += 4)
+        *reinterpret_cast<float4*>(out + c0 + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTile);
 }
 
 // ---------------------------------------------------------------------------
@@ -810,6 +909,8 @@ int curdkv_prepare(evict_handle*) {
           cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem)) !=
           cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramTcSmem)) !=
+          cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)sizeof(EigSmem))) != cudaSuccess)
     return cuda_fail(e, "CurDKV kernel attributes");
@@ -864,7 +965,7 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention pass 2 launch");
   e = timed_launch(h, kKidCurdkvGram, [&] {
-    curdkv_gram_kernel<<<dim3((n + kGramRows - 1) / kGramRows, bh), kGramThreads, 0, sm>>>(p);
+    curdkv_gram_kernel<<<dim3((n + kGramRows - 1) / kGramRows, bh), kAttnThreads, kGramTcSmem, sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV Gram launch");
