@@ -21,6 +21,7 @@ enum KernelId : int {
   kKidCalibGram,
   kKidCalibEig,
   kKidCurdkvLse,
+  kKidCurdkvLseMerge,
   kKidCurdkvColsum,
   kKidCurdkvGram,
   kKidCurdkvEig,

@@ -16,10 +16,11 @@
 // and compaction.
 //
 // Kernels:
-//   curdkv_lse_kernel      pass 1: per query, log2-sum-exp over the keys it sees
-//                          (tcgen05 MMA, 128 queries x 128 keys per step, fp32 in TMEM)
-//   curdkv_colsum_kernel   pass 2: per key, sum over queries of 2^(logit*c - lse)
-//                          (tcgen05 MMA, 128 keys x 128 queries per step)
+//   curdkv_lse_kernel      pass 1: per query and key split, running max and sum of
+//                          2^logit (tcgen05 MMA 128 queries x 128 keys, pipelined)
+//   curdkv_lse_merge_kernel  log2-sum-exp per query from the splits
+//   curdkv_colsum_kernel   pass 2: per key, sum over queries of 2^(logit - lse)
+//                          (tcgen05 MMA 128 keys x 128 queries, pipelined)
 //   curdkv_gram_kernel     partial G over a slice of rows (tcgen05, split bf16)
 //   curdkv_eig_kernel      sum of partials (fp64), Householder tridiagonalisation,
 //                          multisection bisection for the top r eigenvalues,
@@ -43,7 +44,10 @@
 namespace evict {
 
 struct CurdkvState {
-  float* lse = nullptr;        // [BH, max_block]   log2-sum-exp per query
+  float* lse = nullptr;        // [BH, lse_stride]  log2-sum-exp per query
+  float2* lse_part = nullptr;  // [BH, 8, lse_stride] per-split (max, sum)
+  int lse_stride = 0;          // max_block rounded up to 4 (16-byte rows)
+  int sm_count = 0;
   float* attn = nullptr;       // [BH, rows]        column sums
   float* lev = nullptr;        // [BH, rows]        leverage of the last call
   float* gram_part = nullptr;  // [BH, splits, 128*128]
@@ -59,7 +63,6 @@ namespace {
 constexpr int kTile = 128;                  // rows of a query or key tile
 constexpr int kAttnThreads = 128;           // 4 warps: one TMEM lane per thread
 constexpr int kTileBytes = kTile * kHeadDim * 2;
-constexpr int kAttnSmem = 2 * kTileBytes + 1024 + 1024;   // two tiles + alignment + small arrays
 constexpr int kGramRows = 2048;             // rows per Gram partial
 constexpr int kEigThreads = 1024;
 constexpr int kMbarSpin = 1 << 22;          // bounded MMA wait (well above a tile's time)
@@ -73,7 +76,8 @@ struct CurdkvParams {
   int k, m, n, cap, heads, rank;
   float scale2;          // log2(e) / sqrt(D)
   float* lse;
-  int lse_stride;
+  float2* lse_part;       // [BH, kMaxLseSplit, lse_stride] per-split (max, sum)
+  int lse_stride;         // max_block rounded up to 4
   float* attn;
   float* lev;
   int rows;
@@ -105,17 +109,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Load key rows [row0, row0 + 128) (rows >= row_end are zero) into a swizzled tile.
-__device__ __forceinline__ void load_key_tile(const CurdkvParams& p, int bh, uint32_t tile, int row0, int row_end) {
-  for (int c = threadIdx.x; c < kTile * 16; c += kAttnThreads) {
-    const int r = c >> 4, j = c & 15;
-    const int row = row0 + r;
-    const bool ok = row < row_end;
-    const char* src = key_row(p, bh, ok ? row : 0) + j * 16;
-    tc::cp_async16(tile + tc::sw128_offset(r, j, kTile), src, ok ? 16u : 0u);
-  }
-}
-
 // Wait for an MMA commit (bounded); returns false on timeout.
 __device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity, int* err) {
   for (int spin = 0; spin < kMbarSpin; ++spin)
@@ -135,156 +128,291 @@ __device__ __forceinline__ void issue_tile_mma(uint32_t tmem, uint32_t a, uint32
 }
 
 // ---------------------------------------------------------------------------
-// Pass 1: lse2[t] = log2 sum_{i <= k+t} 2^(scale2 * q_t . k_i)
-// grid = (ceil(m / 128), B*H), block = 128
+// Pipelined attention passes. Both use 512 threads: warp w reads TMEM lanes
+// 32*(w%4)..+31 (one accumulator row per thread) and columns 32*(w/4)..+31,
+// a 3-stage cp.async ring for the streamed operand, and two TMEM
+// accumulators so the MMA of tile i+1 runs while tile i is being read.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kAttnThreads) curdkv_lse_kernel(const __grid_constant__ CurdkvParams p) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t bar;
-  __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
-  const int bh = blockIdx.y, t0 = blockIdx.x * kTile;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t q_tile = tc::smem_u32(smem), k_tile = q_tile + kTileBytes;
-  const int t_last = min(p.m, t0 + kTile) - 1;
-  const int key_end = p.k + t_last + 1;          // keys any query of this tile may see
+constexpr int kPipeThreads = 512;
+constexpr int kColGroups = kPipeThreads / kTile;      // warpgroups, each owning 32 columns
+constexpr int kStages = 3;
+constexpr int kPipeSmem = (1 + kStages) * kTileBytes + 1024;
+constexpr int kMaxLseSplit = 8;
 
-  if (tid == 0) {
-    tc::mbar_init(&bar, 1);
-    s_fail = 0;
-  }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, kTile);
-  // queries: incoming rows t0 .. t0+127 (row k + t of the concatenation)
-  for (int c = tid; c < kTile * 16; c += kAttnThreads) {
+// cp.async of one 128-row tile (rows >= row_end are zero) by all threads.
+__device__ __forceinline__ void pipe_load_rows(const CurdkvParams& p, int bh, uint32_t tile, int row0, int row_end) {
+#pragma unroll
+  for (int q = 0; q < kTile * 16 / kPipeThreads; ++q) {
+    const int c = threadIdx.x + q * kPipeThreads;
     const int r = c >> 4, j = c & 15;
-    const bool ok = t0 + r < p.m;
-    const char* src = key_row(p, bh, p.k + (ok ? t0 + r : 0)) + j * 16;
-    tc::cp_async16(q_tile + tc::sw128_offset(r, j, kTile), src, ok ? 16u : 0u);
+    const int row = row0 + r;
+    const bool ok = row < row_end;
+    const char* src = key_row(p, bh, ok ? row : 0) + j * 16;
+    tc::cp_async16(tile + tc::sw128_offset(r, j, kTile), src, ok ? 16u : 0u);
   }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_base;
-  const int t = t0 + tid;                        // this thread's query
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-  float run_max = -INFINITY, run_sum = 0.f;
-  uint32_t parity = 0;
-  for (int i0 = 0; i0 < key_end; i0 += kTile) {
-    load_key_tile(p, bh, k_tile, i0, key_end);
-    tc::cp_async_wait_all();
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc::fence_after_sync();
-      issue_tile_mma(tmem, q_tile, k_tile);
-      tc::mma_commit(&bar);
-    }
-    if (!wait_mma(&bar, parity, p.err)) s_fail = 1;
-    parity ^= 1u;
-    __syncthreads();                               // s_fail is uniform below
-    tc::fence_after_sync();
-    if (!s_fail) {
-#pragma unroll 1
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(trow + c0, v);
-        float cmax = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int i = i0 + c0 + c;
-          v[c] = (t < p.m && i <= p.k + t) ? v[c] * p.scale2 : -INFINITY;
-          cmax = fmaxf(cmax, v[c]);
-        }
-        if (cmax > -INFINITY) {
-          const float nm = fmaxf(run_max, cmax);
-          run_sum = run_max > -INFINITY ? run_sum * ex2(run_max - nm) : 0.f;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) run_sum += ex2(v[c] - nm);
-          run_max = nm;
-        }
-      }
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    if (s_fail) break;
-  }
-  if (!s_fail && t < p.m) p.lse[(size_t)bh * p.lse_stride + t] = run_max + log2f(run_sum);
-  __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, kTile);
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Warp-uniform bounded wait for an MMA commit; every lane returns the same answer.
+__device__ __forceinline__ bool warp_wait_mma(uint64_t* bar, uint32_t parity, int* err) {
+  bool ok = false;
+  for (int spin = 0; spin < kMbarSpin && !ok; ++spin) ok = tc::mbar_try_wait(bar, parity);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (threadIdx.x & 31) == 0) raise_device_error(err, kDevWaitTimeout);
+  return ok;
 }
 
 // ---------------------------------------------------------------------------
-// Pass 2: attn[i] = sum_{t : k+t >= i} 2^(scale2 * q_t . k_i - lse2[t])
-// grid = (ceil(n / 128), B*H), block = 128
+// Pass 1 (split over keys): for query t of the tile and key split s,
+//   (m, s) = (max_i x_i, sum_i 2^(x_i - max)),  x_i = scale2 * q_t . k_i,
+// over the split's share of the keys i <= k + t. grid = (q_tiles, S, B*H).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kAttnThreads) curdkv_colsum_kernel(const __grid_constant__ CurdkvParams p) {
+__global__ void __launch_bounds__(kPipeThreads, 1) curdkv_lse_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar[2];
   __shared__ uint32_t tmem_base;
-  __shared__ float s_lse[kTile];
   __shared__ int s_fail;
-  const int bh = blockIdx.y, i0 = blockIdx.x * kTile;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  __shared__ float s_m[kColGroups][kTile], s_s[kColGroups][kTile];
+  const int t0 = blockIdx.x * kTile, split = blockIdx.y, n_split = gridDim.y, bh = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = 32 * (warp & 3) + lane, grp = warp >> 2;   // accumulator row, column group
+  const int t = t0 + row;
+  const int t_last = min(p.m, t0 + kTile) - 1;
+  const int key_end = p.k + t_last + 1;
+  const int n_kt = (key_end + kTile - 1) / kTile;
+  const int per = (n_kt + n_split - 1) / n_split;
+  const int kt_begin = split * per, kt_end = min(n_kt, kt_begin + per);
+  float2* part = p.lse_part + ((size_t)bh * kMaxLseSplit + split) * p.lse_stride;
+  if (kt_begin >= kt_end) {                        // nothing to see in this split
+    if (grp == 0 && t < p.m) part[t] = make_float2(-INFINITY, 0.f);
+    return;
+  }
+  const int T = kt_end - kt_begin;
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t k_tile = tc::smem_u32(smem), q_tile = k_tile + kTileBytes;
-  const int key_end = min(p.n, i0 + kTile);
-  const int t_first = max(0, i0 - p.k);            // first query that sees a key of this tile
-
+  const uint32_t q_tile = tc::smem_u32(smem), stage0 = q_tile + kTileBytes;
   if (tid == 0) {
-    tc::mbar_init(&bar, 1);
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
     s_fail = 0;
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, kTile);
-  load_key_tile(p, bh, k_tile, i0, key_end);
+  if (warp == 0) tc::tmem_alloc(&tmem_base, 2 * kTile);
+  pipe_load_rows(p, bh, q_tile, p.k + t0, p.k + p.m);              // queries = incoming rows
+  cp_async_commit();
+  pipe_load_rows(p, bh, stage0, kt_begin * kTile, key_end);
+  cp_async_commit();
+  if (T > 1) pipe_load_rows(p, bh, stage0 + kTileBytes, (kt_begin + 1) * kTile, key_end);
+  cp_async_commit();
+  cp_async_wait_1();
+  tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const int i = i0 + tid;                          // this thread's key
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-  const float* lse = p.lse + (size_t)bh * p.lse_stride;
-  float acc = 0.f;
-  uint32_t parity = 0;
-  for (int tq = (t_first / kTile) * kTile; tq < p.m; tq += kTile) {
-    for (int c = tid; c < kTile * 16; c += kAttnThreads) {
-      const int r = c >> 4, j = c & 15;
-      const bool ok = tq + r < p.m;
-      const char* src = key_row(p, bh, p.k + (ok ? tq + r : 0)) + j * 16;
-      tc::cp_async16(q_tile + tc::sw128_offset(r, j, kTile), src, ok ? 16u : 0u);
-    }
-    s_lse[tid] = tq + tid < p.m ? lse[tq + tid] : 0.f;
-    tc::cp_async_wait_all();
+  if (tid == 0) {
+    issue_tile_mma(tmem, q_tile, stage0);
+    tc::mma_commit(&bar[0]);
+  }
+  const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
+  float run_max = -INFINITY, run_sum = 0.f;
+  int consumed = 0, issued = 1;
+  for (int it = 0; it < T; ++it) {
+    if (it + 2 < T) pipe_load_rows(p, bh, stage0 + ((it + 2) % kStages) * kTileBytes, (kt_begin + it + 2) * kTile, key_end);
+    cp_async_commit();
+    cp_async_wait_1();
     tc::fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc::fence_after_sync();
-      issue_tile_mma(tmem, k_tile, q_tile);
-      tc::mma_commit(&bar);
-    }
-    if (!wait_mma(&bar, parity, p.err)) s_fail = 1;
-    parity ^= 1u;
-    __syncthreads();                               // s_fail is uniform below
-    tc::fence_after_sync();
-    if (!s_fail) {
-#pragma unroll 1
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(trow + c0, v);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int tt = tq + c0 + c;
-          if (tt < p.m && i < key_end && i <= p.k + tt) acc += ex2(fmaf(v[c], p.scale2, -s_lse[c0 + c]));
-        }
-      }
-    }
     tc::fence_before_sync();
     __syncthreads();
     if (s_fail) break;
+    if (it + 1 < T) {
+      if (tid == 0) {
+        tc::fence_after_sync();
+        issue_tile_mma(tmem + (uint32_t)(((it + 1) & 1) * kTile), q_tile,
+                       stage0 + ((it + 1) % kStages) * kTileBytes);
+        tc::mma_commit(&bar[(it + 1) & 1]);
+      }
+      ++issued;
+    }
+    if (!warp_wait_mma(&bar[it & 1], (uint32_t)((it >> 1) & 1), p.err)) {
+      if (lane == 0) s_fail = 1;
+      continue;                                    // the next barrier sees s_fail
+    }
+    ++consumed;
+    tc::fence_after_sync();
+    const int i0 = (kt_begin + it) * kTile;
+    const bool full = i0 + kTile - 1 <= p.k + t0;  // every key of the tile is visible to every query
+    const uint32_t acc = tmem + (uint32_t)((it & 1) * kTile) + tlane + (uint32_t)(32 * grp);
+    float v[32];
+    tc::tmem_ld32(acc, v);
+    if (!full) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (i0 + 32 * grp + c > p.k + t) v[c] = -INFINITY;
+    }
+    float mx[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(v[c], v[c + 8]), fmaxf(v[c + 16], v[c + 24]));
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+    if (mx[0] > -INFINITY) {
+      const float nm = fmaxf(run_max, mx[0] * p.scale2);
+      float sm[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sm[q] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) sm[c & 3] += ex2(fmaf(v[c], p.scale2, -nm));
+      run_sum = (run_max > -INFINITY ? run_sum * ex2(run_max - nm) : 0.f) + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
+      run_max = nm;
+    }
+    tc::fence_before_sync();
   }
-  if (!s_fail && i < key_end) p.attn[(size_t)bh * p.rows + i] = acc;
+  // a failure can leave one MMA in flight: wait for it (bounded) before freeing TMEM
+  if (issued > consumed) warp_wait_mma(&bar[consumed & 1], (uint32_t)((consumed >> 1) & 1), p.err);
+  s_m[grp][row] = run_max;
+  s_s[grp][row] = run_sum;
+  tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, kTile);
+  if (grp == 0 && !s_fail && t < p.m) {
+    float mm = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < kColGroups; ++g) mm = fmaxf(mm, s_m[g][row]);
+    float ss = 0.f;
+    if (mm > -INFINITY) {
+#pragma unroll
+      for (int g = 0; g < kColGroups; ++g)
+        if (s_m[g][row] > -INFINITY) ss += s_s[g][row] * ex2(s_m[g][row] - mm);
+    }
+    part[t] = make_float2(mm, ss);
+  }
+  if (warp == 0) tc::tmem_dealloc(tmem, 2 * kTile);
+}
+
+// Merge the key splits: lse2[t] = log2 sum_s s_s 2^(m_s). grid = ceil(m / 256) x B*H.
+__global__ void __launch_bounds__(256) curdkv_lse_merge_kernel(const __grid_constant__ CurdkvParams p, int n_split) {
+  const int bh = blockIdx.y, t = blockIdx.x * 256 + threadIdx.x;
+  if (t >= p.m) return;
+  const float2* part = p.lse_part + (size_t)bh * kMaxLseSplit * p.lse_stride + t;
+  float mm = -INFINITY;
+  for (int s = 0; s < n_split; ++s) mm = fmaxf(mm, part[(size_t)s * p.lse_stride].x);
+  float ss = 0.f;
+  for (int s = 0; s < n_split; ++s) {
+    const float2 v = part[(size_t)s * p.lse_stride];
+    if (v.x > -INFINITY) ss += v.y * ex2(v.x - mm);
+  }
+  p.lse[(size_t)bh * p.lse_stride + t] = mm + log2f(ss);
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: attn[i] = sum_{t : k+t >= i} 2^(scale2 * q_t . k_i - lse2[t]).
+// The key tile is fixed (MMA operand A); query tiles stream through the ring
+// with their lse2 values. grid = (ceil(n / 128), B*H).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPipeThreads, 1) curdkv_colsum_kernel(const __grid_constant__ CurdkvParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t bar[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_fail;
+  __shared__ __align__(16) float s_lse[kStages][kTile];
+  __shared__ float s_acc[kColGroups][kTile];
+  const int i0 = blockIdx.x * kTile, bh = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = 32 * (warp & 3) + lane, grp = warp >> 2;   // accumulator row, column group
+  const int i = i0 + row;                          // this thread's key
+  const int key_end = min(p.n, i0 + kTile);
+  const int t_first = max(0, i0 - p.k);            // first query that sees a key of this tile
+  const int tq0 = (t_first / kTile) * kTile;
+  const int T = (p.m - tq0 + kTile - 1) / kTile;   // >= 1: the last key is seen by the last query
+  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t k_tile = tc::smem_u32(smem), stage0 = k_tile + kTileBytes;
+  const float* lse = p.lse + (size_t)bh * p.lse_stride;
+  auto load_stage = [&](int it) {
+    const int tq = tq0 + it * kTile, st = it % kStages;
+    pipe_load_rows(p, bh, stage0 + st * kTileBytes, p.k + tq, p.k + p.m);
+    if (tid < kTile / 4) {
+      const bool ok = tq + 4 * tid < p.m;          // values past m are never read
+      tc::cp_async16(tc::smem_u32(&s_lse[st][4 * tid]), lse + (ok ? tq + 4 * tid : 0), ok ? 16u : 0u);
+    }
+  };
+  if (tid == 0) {
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
+    s_fail = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, 2 * kTile);
+  pipe_load_rows(p, bh, k_tile, i0, key_end);
+  cp_async_commit();
+  load_stage(0);
+  cp_async_commit();
+  if (T > 1) load_stage(1);
+  cp_async_commit();
+  cp_async_wait_1();
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  if (tid == 0) {
+    issue_tile_mma(tmem, k_tile, stage0);
+    tc::mma_commit(&bar[0]);
+  }
+  const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
+  float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+  int consumed = 0, issued = 1;
+  for (int it = 0; it < T; ++it) {
+    if (it + 2 < T) load_stage(it + 2);
+    cp_async_commit();
+    cp_async_wait_1();
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (s_fail) break;
+    if (it + 1 < T) {
+      if (tid == 0) {
+        tc::fence_after_sync();
+        issue_tile_mma(tmem + (uint32_t)(((it + 1) & 1) * kTile), k_tile,
+                       stage0 + ((it + 1) % kStages) * kTileBytes);
+        tc::mma_commit(&bar[(it + 1) & 1]);
+      }
+      ++issued;
+    }
+    if (!warp_wait_mma(&bar[it & 1], (uint32_t)((it >> 1) & 1), p.err)) {
+      if (lane == 0) s_fail = 1;
+      continue;
+    }
+    ++consumed;
+    tc::fence_after_sync();
+    const int tq = tq0 + it * kTile;
+    const float* l = s_lse[it % kStages] + 32 * grp;
+    // every query of the tile exists and sees every key of the tile
+    const bool full = tq + kTile <= p.m && i0 + kTile - 1 <= p.k + tq;
+    const uint32_t acc = tmem + (uint32_t)((it & 1) * kTile) + tlane + (uint32_t)(32 * grp);
+    float v[32];
+    tc::tmem_ld32(acc, v);
+    if (full) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) acc4[c & 3] += ex2(fmaf(v[c], p.scale2, -l[c]));
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int tt = tq + 32 * grp + c;
+        if (tt < p.m && i <= p.k + tt) acc4[c & 3] += ex2(fmaf(v[c], p.scale2, -l[c]));
+      }
+    }
+    tc::fence_before_sync();
+  }
+  if (issued > consumed) warp_wait_mma(&bar[consumed & 1], (uint32_t)((consumed >> 1) & 1), p.err);
+  s_acc[grp][row] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (grp == 0 && !s_fail && i < key_end) {
+    float a = 0.f;
+#pragma unroll
+    for (int g = 0; g < kColGroups; ++g) a += s_acc[g][row];
+    p.attn[(size_t)bh * p.rows + i] = a;
+  }
+  if (warp == 0) tc::tmem_dealloc(tmem, 2 * kTile);
 }
 
 // ---------------------------------------------------------------------------
@@ -890,7 +1018,9 @@ void curdkv_layout(evict_handle* h, size_t* off, char* base) {
     *off += bytes;
     return p;
   };
-  st.lse = reinterpret_cast<float*>(take(bh * h->cfg.max_block * 4));
+  st.lse_stride = (h->cfg.max_block + 3) / 4 * 4;
+  st.lse = reinterpret_cast<float*>(take(bh * st.lse_stride * 4));
+  st.lse_part = reinterpret_cast<float2*>(take(bh * kMaxLseSplit * st.lse_stride * sizeof(float2)));
   st.attn = reinterpret_cast<float*>(take(bh * st.rows * 4));
   st.lev = reinterpret_cast<float*>(take(bh * st.rows * 4));
   st.gram_part = reinterpret_cast<float*>(take(bh * st.splits * kHeadDim * kHeadDim * 4));
@@ -903,11 +1033,14 @@ void curdkv_release(evict_handle* h) {
   h->curdkv = nullptr;
 }
 
-int curdkv_prepare(evict_handle*) {
+int curdkv_prepare(evict_handle* h) {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(curdkv_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem)) !=
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&h->curdkv->sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(curdkv_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem)) !=
+      (e = cudaFuncSetAttribute(curdkv_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramTcSmem)) !=
           cudaSuccess ||
@@ -936,7 +1069,8 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   p.rank = std::min(std::min(c.rank_cap, n), kHeadDim);
   p.scale2 = kLog2e / sqrtf((float)kHeadDim);
   p.lse = st.lse;
-  p.lse_stride = c.max_block;
+  p.lse_part = st.lse_part;
+  p.lse_stride = st.lse_stride;
   p.attn = st.attn;
   p.lev = st.lev;
   p.rows = st.rows;
@@ -954,13 +1088,22 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   const cudaStream_t sm = h->stream;
   cudaError_t e;
   const int q_tiles = (m + kTile - 1) / kTile, k_tiles = (n + kTile - 1) / kTile;
+  // key splits for pass 1: enough CTAs to fill the GPU a few times over,
+  // each split keeping at least 4 key tiles
+  int n_split = (4 * std::max(st.sm_count, 1) + q_tiles * bh - 1) / (q_tiles * bh);
+  n_split = std::max(1, std::min({n_split, kMaxLseSplit, std::max(1, k_tiles / 4)}));
   e = timed_launch(h, kKidCurdkvLse, [&] {
-    curdkv_lse_kernel<<<dim3(q_tiles, bh), kAttnThreads, kAttnSmem, sm>>>(p);
+    curdkv_lse_kernel<<<dim3(q_tiles, n_split, bh), kPipeThreads, kPipeSmem, sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention pass 1 launch");
+  e = timed_launch(h, kKidCurdkvLseMerge, [&] {
+    curdkv_lse_merge_kernel<<<dim3((m + 255) / 256, bh), 256, 0, sm>>>(p, n_split);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention merge launch");
   e = timed_launch(h, kKidCurdkvColsum, [&] {
-    curdkv_colsum_kernel<<<dim3(k_tiles, bh), kAttnThreads, kAttnSmem, sm>>>(p);
+    curdkv_colsum_kernel<<<dim3(k_tiles, bh), kPipeThreads, kPipeSmem, sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention pass 2 launch");

@@ -41,7 +41,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 const char* const kKernelNames[kKidCount] = {
     "score", "score_append", "select", "compact", "calib_gram", "calib_eig",
-    "curdkv_lse", "curdkv_colsum", "curdkv_gram", "curdkv_eig", "curdkv_leverage",
+    "curdkv_lse", "curdkv_lse_merge", "curdkv_colsum", "curdkv_gram", "curdkv_eig", "curdkv_leverage",
 };
 
 cudaEvent_t take_event(evict_handle* h) {
