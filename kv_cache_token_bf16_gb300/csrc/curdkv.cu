@@ -17,10 +17,10 @@
 //
 // Kernels:
 //   curdkv_lse_kernel      pass 1: per query and key split, running max and sum of
-//                          2^logit (tcgen05 MMA 128 queries x 128 keys, pipelined)
+//                          2^logit (tcgen05 MMA, 256 queries x 128 keys per step, pipelined)
 //   curdkv_lse_merge_kernel  log2-sum-exp per query from the splits
 //   curdkv_colsum_kernel   pass 2: per key, sum over queries of 2^(logit - lse)
-//                          (tcgen05 MMA 128 keys x 128 queries, pipelined)
+//                          (tcgen05 MMA, 256 keys x 128 queries per step, pipelined)
 //   curdkv_gram_kernel     partial G over a slice of rows (tcgen05, split bf16)
 //   curdkv_eig_kernel      sum of partials (fp64), Householder tridiagonalisation,
 //                          multisection bisection for the top r eigenvalues,
@@ -128,15 +128,18 @@ __device__ __forceinline__ void issue_tile_mma(uint32_t tmem, uint32_t a, uint32
 }
 
 // ---------------------------------------------------------------------------
-// Pipelined attention passes. Both use 512 threads: warp w reads TMEM lanes
-// 32*(w%4)..+31 (one accumulator row per thread) and columns 32*(w/4)..+31,
-// a 3-stage cp.async ring for the streamed operand, and two TMEM
-// accumulators so the MMA of tile i+1 runs while tile i is being read.
+// Pipelined attention passes. Each CTA holds two fixed 128-row operand tiles
+// (256 queries in pass 1, 256 keys in pass 2) and streams the other operand
+// through a 3-stage cp.async ring; every streamed tile feeds two 128 x 128
+// MMAs. TMEM holds two buffers of two fp32 accumulators (512 columns), so
+// the MMAs of tile i+1 run while tile i is read. 512 threads: warp w reads
+// TMEM lanes 32*(w%4)..+31 (one accumulator row per thread) and, with
+// g = w/4, accumulator g/2, columns 64*(g%2)..+63.
 // ---------------------------------------------------------------------------
 constexpr int kPipeThreads = 512;
-constexpr int kColGroups = kPipeThreads / kTile;      // warpgroups, each owning 32 columns
+constexpr int kColGroups = 4;                     // column groups of 64 over the two accumulators
 constexpr int kStages = 3;
-constexpr int kPipeSmem = (1 + kStages) * kTileBytes + 1024;
+constexpr int kPipeSmem = (2 + kStages) * kTileBytes + 1024;
 constexpr int kMaxLseSplit = 8;
 
 // cp.async of one 128-row tile (rows >= row_end are zero) by all threads.
@@ -163,10 +166,21 @@ __device__ __forceinline__ bool warp_wait_mma(uint64_t* bar, uint32_t parity, in
   return ok;
 }
 
+// MMAs of one streamed tile into buffer `buf`: accumulator a = fixed tile a x streamed tile.
+// `two` = the second fixed tile holds real rows. Pass 1 puts the fixed tiles
+// on the A side (rows = queries), pass 2 too (rows = keys).
+__device__ __forceinline__ void issue_pair(uint32_t tmem, int buf, uint32_t fixed0, uint32_t streamed, bool two,
+                                           uint64_t* bar) {
+  tc::fence_after_sync();
+  issue_tile_mma(tmem + (uint32_t)(buf * 2 * kTile), fixed0, streamed);
+  if (two) issue_tile_mma(tmem + (uint32_t)(buf * 2 * kTile + kTile), fixed0 + kTileBytes, streamed);
+  tc::mma_commit(bar);
+}
+
 // ---------------------------------------------------------------------------
-// Pass 1 (split over keys): for query t of the tile and key split s,
+// Pass 1 (split over keys): for query t of the CTA's 256 and key split s,
 //   (m, s) = (max_i x_i, sum_i 2^(x_i - max)),  x_i = scale2 * q_t . k_i,
-// over the split's share of the keys i <= k + t. grid = (q_tiles, S, B*H).
+// over the split's share of the keys i <= k + t. grid = (ceil(m/256), S, B*H).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_lse_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -174,30 +188,33 @@ __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_lse_kernel(const __gri
   __shared__ uint32_t tmem_base;
   __shared__ int s_fail;
   __shared__ float s_m[kColGroups][kTile], s_s[kColGroups][kTile];
-  const int t0 = blockIdx.x * kTile, split = blockIdx.y, n_split = gridDim.y, bh = blockIdx.z;
+  const int t0 = blockIdx.x * 2 * kTile, split = blockIdx.y, n_split = gridDim.y, bh = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = 32 * (warp & 3) + lane, grp = warp >> 2;   // accumulator row, column group
-  const int t = t0 + row;
-  const int t_last = min(p.m, t0 + kTile) - 1;
+  const int g = warp >> 2, a = g >> 1, col0 = 64 * (g & 1);
+  const int row = 32 * (warp & 3) + lane;
+  const int t = t0 + a * kTile + row;                // this thread's query
+  const bool two = t0 + kTile < p.m;                 // the second query tile exists
+  const int t_last = min(p.m, t0 + 2 * kTile) - 1;
   const int key_end = p.k + t_last + 1;
   const int n_kt = (key_end + kTile - 1) / kTile;
   const int per = (n_kt + n_split - 1) / n_split;
   const int kt_begin = split * per, kt_end = min(n_kt, kt_begin + per);
   float2* part = p.lse_part + ((size_t)bh * kMaxLseSplit + split) * p.lse_stride;
-  if (kt_begin >= kt_end) {                        // nothing to see in this split
-    if (grp == 0 && t < p.m) part[t] = make_float2(-INFINITY, 0.f);
+  if (kt_begin >= kt_end) {                          // nothing to see in this split
+    if ((g & 1) == 0 && t < p.m) part[t] = make_float2(-INFINITY, 0.f);
     return;
   }
   const int T = kt_end - kt_begin;
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t q_tile = tc::smem_u32(smem), stage0 = q_tile + kTileBytes;
+  const uint32_t q_tiles = tc::smem_u32(smem), stage0 = q_tiles + 2 * kTileBytes;
   if (tid == 0) {
     tc::mbar_init(&bar[0], 1);
     tc::mbar_init(&bar[1], 1);
     s_fail = 0;
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, 2 * kTile);
-  pipe_load_rows(p, bh, q_tile, p.k + t0, p.k + p.m);              // queries = incoming rows
+  if (warp == 0) tc::tmem_alloc(&tmem_base, 4 * kTile);
+  pipe_load_rows(p, bh, q_tiles, p.k + t0, p.k + p.m);                  // queries = incoming rows
+  pipe_load_rows(p, bh, q_tiles + kTileBytes, p.k + t0 + kTile, p.k + p.m);
   cp_async_commit();
   pipe_load_rows(p, bh, stage0, kt_begin * kTile, key_end);
   cp_async_commit();
@@ -209,11 +226,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_lse_kernel(const __gri
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  if (tid == 0) {
-    issue_tile_mma(tmem, q_tile, stage0);
-    tc::mma_commit(&bar[0]);
-  }
+  if (tid == 0) issue_pair(tmem, 0, q_tiles, stage0, two, &bar[0]);
   const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
+  const bool active = a == 0 || two;                 // warp-uniform: this warp's accumulator exists
   float run_max = -INFINITY, run_sum = 0.f;
   int consumed = 0, issued = 1;
   for (int it = 0; it < T; ++it) {
@@ -225,68 +240,63 @@ __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_lse_kernel(const __gri
     __syncthreads();
     if (s_fail) break;
     if (it + 1 < T) {
-      if (tid == 0) {
-        tc::fence_after_sync();
-        issue_tile_mma(tmem + (uint32_t)(((it + 1) & 1) * kTile), q_tile,
-                       stage0 + ((it + 1) % kStages) * kTileBytes);
-        tc::mma_commit(&bar[(it + 1) & 1]);
-      }
+      if (tid == 0) issue_pair(tmem, (it + 1) & 1, q_tiles, stage0 + ((it + 1) % kStages) * kTileBytes, two,
+                               &bar[(it + 1) & 1]);
       ++issued;
     }
     if (!warp_wait_mma(&bar[it & 1], (uint32_t)((it >> 1) & 1), p.err)) {
       if (lane == 0) s_fail = 1;
-      continue;                                    // the next barrier sees s_fail
+      continue;                                      // the next barrier sees s_fail
     }
     ++consumed;
     tc::fence_after_sync();
-    const int i0 = (kt_begin + it) * kTile;
-    const bool full = i0 + kTile - 1 <= p.k + t0;  // every key of the tile is visible to every query
-    const uint32_t acc = tmem + (uint32_t)((it & 1) * kTile) + tlane + (uint32_t)(32 * grp);
-    float v[32];
-    tc::tmem_ld32(acc, v);
-    if (!full) {
+    if (active) {
+      const int i0 = (kt_begin + it) * kTile;
+      const bool full = i0 + kTile - 1 <= p.k + t0 + a * kTile;   // every key visible to every query
+      const uint32_t acc = tmem + (uint32_t)((it & 1) * 2 * kTile + a * kTile + col0) + tlane;
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (i0 + 32 * grp + c > p.k + t) v[c] = -INFINITY;
-    }
-    float mx[8];
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(acc + c0, v);
+        if (!full) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(v[c], v[c + 8]), fmaxf(v[c + 16], v[c + 24]));
+          for (int c = 0; c < 32; ++c)
+            if (i0 + col0 + c0 + c > p.k + t) v[c] = -INFINITY;
+        }
+        float mx[8];
 #pragma unroll
-    for (int w = 4; w >= 1; w >>= 1)
+        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(v[c], v[c + 8]), fmaxf(v[c + 16], v[c + 24]));
 #pragma unroll
-      for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
-    if (mx[0] > -INFINITY) {
-      const float nm = fmaxf(run_max, mx[0] * p.scale2);
-      float sm[4];
+        for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sm[q] = 0.f;
+          for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+        if (mx[0] > -INFINITY) {
+          const float nm = fmaxf(run_max, mx[0] * p.scale2);
+          float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) sm[c & 3] += ex2(fmaf(v[c], p.scale2, -nm));
-      run_sum = (run_max > -INFINITY ? run_sum * ex2(run_max - nm) : 0.f) + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
-      run_max = nm;
+          for (int c = 0; c < 32; ++c) sm[c & 3] += ex2(fmaf(v[c], p.scale2, -nm));
+          run_sum = (run_max > -INFINITY ? run_sum * ex2(run_max - nm) : 0.f) + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
+          run_max = nm;
+        }
+      }
     }
     tc::fence_before_sync();
   }
-  // a failure can leave one MMA in flight: wait for it (bounded) before freeing TMEM
+  // a failure can leave MMAs in flight: wait for them (bounded) before freeing TMEM
   if (issued > consumed) warp_wait_mma(&bar[consumed & 1], (uint32_t)((consumed >> 1) & 1), p.err);
-  s_m[grp][row] = run_max;
-  s_s[grp][row] = run_sum;
+  s_m[g][row] = run_max;
+  s_s[g][row] = run_sum;
   tc::fence_before_sync();
   __syncthreads();
-  if (grp == 0 && !s_fail && t < p.m) {
-    float mm = -INFINITY;
-#pragma unroll
-    for (int g = 0; g < kColGroups; ++g) mm = fmaxf(mm, s_m[g][row]);
+  if ((g & 1) == 0 && active && !s_fail && t < p.m) {
+    const float m0 = s_m[g][row], m1 = s_m[g + 1][row];
+    const float mm = fmaxf(m0, m1);
     float ss = 0.f;
-    if (mm > -INFINITY) {
-#pragma unroll
-      for (int g = 0; g < kColGroups; ++g)
-        if (s_m[g][row] > -INFINITY) ss += s_s[g][row] * ex2(s_m[g][row] - mm);
-    }
+    if (mm > -INFINITY)
+      ss = (m0 > -INFINITY ? s_s[g][row] * ex2(m0 - mm) : 0.f) + (m1 > -INFINITY ? s_s[g + 1][row] * ex2(m1 - mm) : 0.f);
     part[t] = make_float2(mm, ss);
   }
-  if (warp == 0) tc::tmem_dealloc(tmem, 2 * kTile);
+  if (warp == 0) tc::tmem_dealloc(tmem, 4 * kTile);
 }
 
 // Merge the key splits: lse2[t] = log2 sum_s s_s 2^(m_s). grid = ceil(m / 256) x B*H.
@@ -306,8 +316,8 @@ __global__ void __launch_bounds__(256) curdkv_lse_merge_kernel(const __grid_cons
 
 // ---------------------------------------------------------------------------
 // Pass 2: attn[i] = sum_{t : k+t >= i} 2^(scale2 * q_t . k_i - lse2[t]).
-// The key tile is fixed (MMA operand A); query tiles stream through the ring
-// with their lse2 values. grid = (ceil(n / 128), B*H).
+// The CTA's 256 keys are fixed (MMA operand A); query tiles stream through
+// the ring with their lse2 values. grid = (ceil(n / 256), B*H).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_colsum_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -316,16 +326,18 @@ __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_colsum_kernel(const __
   __shared__ int s_fail;
   __shared__ __align__(16) float s_lse[kStages][kTile];
   __shared__ float s_acc[kColGroups][kTile];
-  const int i0 = blockIdx.x * kTile, bh = blockIdx.y;
+  const int i0 = blockIdx.x * 2 * kTile, bh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = 32 * (warp & 3) + lane, grp = warp >> 2;   // accumulator row, column group
-  const int i = i0 + row;                          // this thread's key
-  const int key_end = min(p.n, i0 + kTile);
-  const int t_first = max(0, i0 - p.k);            // first query that sees a key of this tile
+  const int g = warp >> 2, a = g >> 1, col0 = 64 * (g & 1);
+  const int row = 32 * (warp & 3) + lane;
+  const int i = i0 + a * kTile + row;              // this thread's key
+  const int key_end = min(p.n, i0 + 2 * kTile);
+  const bool two = i0 + kTile < p.n;               // the second key tile exists
+  const int t_first = max(0, i0 - p.k);            // first query that sees a key of the CTA
   const int tq0 = (t_first / kTile) * kTile;
   const int T = (p.m - tq0 + kTile - 1) / kTile;   // >= 1: the last key is seen by the last query
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t k_tile = tc::smem_u32(smem), stage0 = k_tile + kTileBytes;
+  const uint32_t k_tiles = tc::smem_u32(smem), stage0 = k_tiles + 2 * kTileBytes;
   const float* lse = p.lse + (size_t)bh * p.lse_stride;
   auto load_stage = [&](int it) {
     const int tq = tq0 + it * kTile, st = it % kStages;
@@ -340,8 +352,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_colsum_kernel(const __
     tc::mbar_init(&bar[1], 1);
     s_fail = 0;
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, 2 * kTile);
-  pipe_load_rows(p, bh, k_tile, i0, key_end);
+  if (warp == 0) tc::tmem_alloc(&tmem_base, 4 * kTile);
+  pipe_load_rows(p, bh, k_tiles, i0, key_end);
+  pipe_load_rows(p, bh, k_tiles + kTileBytes, i0 + kTile, key_end);
   cp_async_commit();
   load_stage(0);
   cp_async_commit();
@@ -353,11 +366,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_colsum_kernel(const __
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  if (tid == 0) {
-    issue_tile_mma(tmem, k_tile, stage0);
-    tc::mma_commit(&bar[0]);
-  }
+  if (tid == 0) issue_pair(tmem, 0, k_tiles, stage0, two, &bar[0]);
   const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
+  const bool active = a == 0 || two;               // warp-uniform: this warp's accumulator exists
+  const int key_base = i0 + a * kTile;             // first key of this warp's accumulator
   float acc4[4] = {0.f, 0.f, 0.f, 0.f};
   int consumed = 0, issued = 1;
   for (int it = 0; it < T; ++it) {
@@ -369,12 +381,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_colsum_kernel(const __
     __syncthreads();
     if (s_fail) break;
     if (it + 1 < T) {
-      if (tid == 0) {
-        tc::fence_after_sync();
-        issue_tile_mma(tmem + (uint32_t)(((it + 1) & 1) * kTile), k_tile,
-                       stage0 + ((it + 1) % kStages) * kTileBytes);
-        tc::mma_commit(&bar[(it + 1) & 1]);
-      }
+      if (tid == 0) issue_pair(tmem, (it + 1) & 1, k_tiles, stage0 + ((it + 1) % kStages) * kTileBytes, two,
+                               &bar[(it + 1) & 1]);
       ++issued;
     }
     if (!warp_wait_mma(&bar[it & 1], (uint32_t)((it >> 1) & 1), p.err)) {
@@ -383,36 +391,36 @@ __global__ void __launch_bounds__(kPipeThreads, 1) curdkv_colsum_kernel(const __
     }
     ++consumed;
     tc::fence_after_sync();
-    const int tq = tq0 + it * kTile;
-    const float* l = s_lse[it % kStages] + 32 * grp;
-    // every query of the tile exists and sees every key of the tile
-    const bool full = tq + kTile <= p.m && i0 + kTile - 1 <= p.k + tq;
-    const uint32_t acc = tmem + (uint32_t)((it & 1) * kTile) + tlane + (uint32_t)(32 * grp);
-    float v[32];
-    tc::tmem_ld32(acc, v);
-    if (full) {
+    if (active) {
+      const int tq = tq0 + it * kTile;
+      const float* l = s_lse[it % kStages] + col0;
+      // every query of the tile exists and sees every key of the accumulator
+      const bool full = tq + kTile <= p.m && key_base + kTile - 1 <= p.k + tq;
+      const uint32_t acc = tmem + (uint32_t)((it & 1) * 2 * kTile + a * kTile + col0) + tlane;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) acc4[c & 3] += ex2(fmaf(v[c], p.scale2, -l[c]));
-    } else {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(acc + c0, v);
+        if (full) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int tt = tq + 32 * grp + c;
-        if (tt < p.m && i <= p.k + tt) acc4[c & 3] += ex2(fmaf(v[c], p.scale2, -l[c]));
+          for (int c = 0; c < 32; ++c) acc4[c & 3] += ex2(fmaf(v[c], p.scale2, -l[c0 + c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int tt = tq + col0 + c0 + c;
+            if (tt < p.m && i <= p.k + tt) acc4[c & 3] += ex2(fmaf(v[c], p.scale2, -l[c0 + c]));
+          }
+        }
       }
     }
     tc::fence_before_sync();
   }
   if (issued > consumed) warp_wait_mma(&bar[consumed & 1], (uint32_t)((consumed >> 1) & 1), p.err);
-  s_acc[grp][row] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+  s_acc[g][row] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
   tc::fence_before_sync();
   __syncthreads();
-  if (grp == 0 && !s_fail && i < key_end) {
-    float a = 0.f;
-#pragma unroll
-    for (int g = 0; g < kColGroups; ++g) a += s_acc[g][row];
-    p.attn[(size_t)bh * p.rows + i] = a;
-  }
-  if (warp == 0) tc::tmem_dealloc(tmem, 2 * kTile);
+  if ((g & 1) == 0 && active && !s_fail && i < key_end) p.attn[(size_t)bh * p.rows + i] = s_acc[g][row] + s_acc[g + 1][row];
+  if (warp == 0) tc::tmem_dealloc(tmem, 4 * kTile);
 }
 
 // ---------------------------------------------------------------------------
@@ -1087,13 +1095,14 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   p.err = h->err;
   const cudaStream_t sm = h->stream;
   cudaError_t e;
-  const int q_tiles = (m + kTile - 1) / kTile, k_tiles = (n + kTile - 1) / kTile;
+  const int k_tiles = (n + kTile - 1) / kTile;
   // key splits for pass 1: enough CTAs to fill the GPU a few times over,
   // each split keeping at least 4 key tiles
-  int n_split = (4 * std::max(st.sm_count, 1) + q_tiles * bh - 1) / (q_tiles * bh);
+  const int q_pairs = (m + 2 * kTile - 1) / (2 * kTile), k_pairs = (n + 2 * kTile - 1) / (2 * kTile);
+  int n_split = (4 * std::max(st.sm_count, 1) + q_pairs * bh - 1) / (q_pairs * bh);
   n_split = std::max(1, std::min({n_split, kMaxLseSplit, std::max(1, k_tiles / 4)}));
   e = timed_launch(h, kKidCurdkvLse, [&] {
-    curdkv_lse_kernel<<<dim3(q_tiles, n_split, bh), kPipeThreads, kPipeSmem, sm>>>(p);
+    curdkv_lse_kernel<<<dim3(q_pairs, n_split, bh), kPipeThreads, kPipeSmem, sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention pass 1 launch");
@@ -1103,7 +1112,7 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention merge launch");
   e = timed_launch(h, kKidCurdkvColsum, [&] {
-    curdkv_colsum_kernel<<<dim3(k_tiles, bh), kPipeThreads, kPipeSmem, sm>>>(p);
+    curdkv_colsum_kernel<<<dim3(k_pairs, bh), kPipeThreads, kPipeSmem, sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention pass 2 launch");
