@@ -25,7 +25,7 @@
 //   curdkv_eig_kernel      sum of partials (fp64), Householder tridiagonalisation,
 //                          multisection bisection for the top r eigenvalues,
 //                          inverse iteration, orthonormalisation, back-transform
-//   curdkv_leverage_kernel l_i and the cumulative-score update
+//   curdkv_leverage_kernel l_i (projections on tcgen05) and the cumulative-score update
 //   curdkv_append_kernel   copy of the block when the cache stays within budget
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -949,44 +949,91 @@ __global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid
 }
 
 // ---------------------------------------------------------------------------
-// Leverage and cumulative score. grid = (ceil(n / 128), B*H), block = 128.
+// Leverage and cumulative score on the tensor cores. One CTA per 128 rows of
+// one (b, h): the projections P = V_tile E^T (E = the top-r eigenvectors,
+// split into bf16 hi + lo, zero rows past r) come from one M=128, N=32 MMA
+// chain with the value tile in its natural K-major layout; then
+// l_i = a_i^2 * |P_i|^2 / E, accumulated into kept rows' scores and seeding
+// incoming rows'. grid = (ceil(n / 128), B*H), block = 128.
 // ---------------------------------------------------------------------------
+constexpr int kEvecTileBytes = kCurdkvMaxRank * kHeadDim * 2;
+constexpr int kLevSmem = kTileBytes + 2 * kEvecTileBytes + 1024;
+static_assert(kCurdkvMaxRank == 32, "the leverage MMA uses N = 32");
+
 __global__ void __launch_bounds__(kAttnThreads) curdkv_leverage_kernel(const __grid_constant__ CurdkvParams p) {
-  __shared__ float ev[kCurdkvMaxRank][kHeadDim];
-  const int bh = blockIdx.y, tid = threadIdx.x;
-  const int r = p.rank;
-  const float* src = p.evec + (size_t)bh * kCurdkvMaxRank * kHeadDim;
-  for (int el = tid; el < r * kHeadDim; el += kAttnThreads) ev[el / kHeadDim][el % kHeadDim] = src[el];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int bh = blockIdx.y, i0 = blockIdx.x * kTile, tid = threadIdx.x, warp = tid >> 5;
+  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t v_tile = tc::smem_u32(smem), ehi = v_tile + kTileBytes, elo = ehi + kEvecTileBytes;
+  const int row_end = min(p.n, i0 + kTile);
+  if (tid == 0) tc::mbar_init(&bar, 1);
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kCurdkvMaxRank);
+  for (int c = tid; c < kTile * 16; c += kAttnThreads) {
+    const int r = c >> 4, j = c & 15;
+    const int row = i0 + r;
+    const bool ok = row < row_end;
+    tc::cp_async16(v_tile + tc::sw128_offset(r, j, kTile), value_row(p, bh, ok ? row : i0) + j * 16, ok ? 16u : 0u);
+  }
+  // eigenvectors -> bf16 hi and lo tiles (32 rows, K-major, swizzled)
+  const float* ev = p.evec + (size_t)bh * kCurdkvMaxRank * kHeadDim;
+  for (int item = tid; item < kCurdkvMaxRank * 16; item += kAttnThreads) {
+    const int jr = item >> 4, ch = item & 15;
+    const float4 x0 = *reinterpret_cast<const float4*>(ev + jr * kHeadDim + 8 * ch);
+    const float4 x1 = *reinterpret_cast<const float4*>(ev + jr * kHeadDim + 8 * ch + 4);
+    const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      hw[q] = pack_bf16x2(x[2 * q], x[2 * q + 1]);
+      lw[q] = pack_bf16x2(x[2 * q] - __uint_as_float(hw[q] << 16), x[2 * q + 1] - __uint_as_float(hw[q] & 0xffff0000u));
+    }
+    const uint32_t off = tc::sw128_offset(jr, ch, kCurdkvMaxRank);
+    *reinterpret_cast<uint4*>(smem + kTileBytes + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(smem + kTileBytes + kEvecTileBytes + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+  tc::cp_async_wait_all();
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
   __syncthreads();
-  const int i = blockIdx.x * kTile + tid;
-  if (i >= p.n) return;
-  const float inv_e = p.inv_e[bh];
-  float proj[kCurdkvMaxRank];
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  if (tid == 0) {
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(kTile, kCurdkvMaxRank);
 #pragma unroll
-  for (int jj = 0; jj < kCurdkvMaxRank; ++jj) proj[jj] = 0.f;
-  const char* vrow = value_row(p, bh, i);
-#pragma unroll 1
-  for (int c = 0; c < 16; ++c) {
-    float x[8];
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(vrow + 16 * c), x);
+    for (int st = 0; st < 8; ++st) {
+      const uint32_t a_off = (uint32_t)((st >> 2) * kTile * 128 + (st & 3) * 32);
+      const uint32_t b_off = (uint32_t)((st >> 2) * kCurdkvMaxRank * 128 + (st & 3) * 32);
+      const uint64_t ad = tc::sw128_desc(v_tile + a_off);
+      tc::mma_bf16(tmem, ad, tc::sw128_desc(ehi + b_off), idesc, st > 0 ? 1u : 0u);
+      tc::mma_bf16(tmem, ad, tc::sw128_desc(elo + b_off), idesc, 1u);
+    }
+    tc::mma_commit(&bar);
+  }
+  bool ok = false;
+  for (int spin = 0; spin < kMbarSpin && !ok; ++spin) ok = tc::mbar_try_wait(&bar, 0);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (tid & 31) == 0) raise_device_error(p.err, kDevWaitTimeout);
+  tc::fence_after_sync();
+  const int i = i0 + tid;
+  if (ok) {
+    float proj[32];
+    tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), proj);
+    float e4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int jj = 0; jj < kCurdkvMaxRank; ++jj) {
-      if (jj < r) {
-        float acc = proj[jj];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc = fmaf(x[q], ev[jj][8 * c + q], acc);
-        proj[jj] = acc;
-      }
+    for (int jj = 0; jj < 32; ++jj) e4[jj & 3] = fmaf(proj[jj], proj[jj], e4[jj & 3]);
+    if (i < p.n) {
+      const float a = p.attn[(size_t)bh * p.rows + i];
+      const float l = a * a * ((e4[0] + e4[1]) + (e4[2] + e4[3])) * p.inv_e[bh];
+      p.lev[(size_t)bh * p.rows + i] = l;
+      if (i < p.k) p.score_st[(size_t)bh * p.cap + i] += l;
+      else p.new_score[(size_t)bh * p.new_stride + (i - p.k)] = l;
     }
   }
-  float e2 = 0.f;
-#pragma unroll
-  for (int jj = 0; jj < kCurdkvMaxRank; ++jj) e2 = fmaf(proj[jj], proj[jj], e2);
-  const float a = p.attn[(size_t)bh * p.rows + i];
-  const float l = a * a * e2 * inv_e;
-  p.lev[(size_t)bh * p.rows + i] = l;
-  if (i < p.k) p.score_st[(size_t)bh * p.cap + i] += l;
-  else p.new_score[(size_t)bh * p.new_stride + (i - p.k)] = l;
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kCurdkvMaxRank);
 }
 
 // Append the block (cache stays within budget): grid = (ceil(m / 64), B*H), block = 256.
@@ -1051,6 +1098,8 @@ int curdkv_prepare(evict_handle* h) {
       (e = cudaFuncSetAttribute(curdkv_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramTcSmem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_leverage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLevSmem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)sizeof(EigSmem))) != cudaSuccess)
@@ -1127,7 +1176,7 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV eigensolver launch");
   e = timed_launch(h, kKidCurdkvLeverage, [&] {
-    curdkv_leverage_kernel<<<dim3(k_tiles, bh), kAttnThreads, 0, sm>>>(p);
+    curdkv_leverage_kernel<<<dim3(k_tiles, bh), kAttnThreads, kLevSmem, sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV leverage launch");
