@@ -128,8 +128,11 @@ int evict_init(const evict_config* cfg, evict_handle** out);
  * NULL (then positions are offset + [0, m)). Scores the incoming keys
  * once, appends, and over budget keeps the protected top-k in temporal
  * order; then offset += m. m == 0 is a no-op returning the current view.
- * EVICT_EINVAL: NULL handle/k/v with m > 0, m < 0, m > max_block, or an
- * append that would exceed capacity without eviction. `out` may be NULL. */
+ * k and v must be 16-byte aligned (they are read with 16-byte vector and
+ * TMA loads) and pos 4-byte aligned.
+ * EVICT_EINVAL: NULL handle/k/v with m > 0, m < 0, m > max_block, a
+ * misaligned k/v/pos, or an append that would exceed capacity without
+ * eviction. `out` may be NULL. */
 int evict_update_and_fetch(evict_handle* h, const void* k, const void* v, const int32_t* pos,
                            int m, evict_view* out);
 

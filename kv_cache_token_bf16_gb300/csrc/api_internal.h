@@ -23,6 +23,7 @@ enum KernelId : int {
   kKidCurdkvLse,
   kKidCurdkvLseMerge,
   kKidCurdkvColsum,
+  kKidCurdkvColsumMerge,
   kKidCurdkvGram,
   kKidCurdkvEig,
   kKidCurdkvLeverage,

@@ -16,17 +16,20 @@
 // and compaction.
 //
 // Kernels:
-//   curdkv_lse_kernel      pass 1: per query and key split, running max and sum of
-//                          2^logit (tcgen05 MMA, 256 queries x 128 keys per step, pipelined)
-//   curdkv_lse_merge_kernel  log2-sum-exp per query from the splits
+//   curdkv_lse_kernel      pass 1: per query, running max and sum of 2^logit over
+//                          this CTA's key tiles (TMA-fed tcgen05 MMA, 512 queries x
+//                          128 keys per step, warp-specialised, persistent grid)
+//   curdkv_lse_merge_kernel  log2-sum-exp per query from the per-CTA partials
 //   curdkv_colsum_kernel   pass 2: per key, sum over queries of 2^(logit - lse)
-//                          (tcgen05 MMA, 256 keys x 128 queries per step, pipelined)
+//                          (same pipeline, 128 keys x 512 queries per step)
+//   curdkv_colsum_merge_kernel  sum of the per-quad column sums (blocks > 512 rows)
 //   curdkv_gram_kernel     partial G over a slice of rows (tcgen05, split bf16)
 //   curdkv_eig_kernel      sum of partials (fp64), Householder tridiagonalisation,
 //                          multisection bisection for the top r eigenvalues,
 //                          inverse iteration, orthonormalisation, back-transform
 //   curdkv_leverage_kernel l_i (projections on tcgen05) and the cumulative-score update
 //   curdkv_append_kernel   copy of the block when the cache stays within budget
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -56,6 +59,8 @@ struct CurdkvState {
   int rows = 0;                // cap + max_block
   int splits = 0;              // gram partials per (b, h)
   int last_n = 0;              // rows of the last update
+  float* colpart = nullptr;    // [quads, BH, rows] per-quad column sums (blocks > 512 rows)
+  int quads = 0;               // ceil(max_block / 512)
 };
 
 namespace {
@@ -68,7 +73,25 @@ constexpr int kEigThreads = 1024;
 constexpr int kMbarSpin = 1 << 22;          // bounded MMA wait (well above a tile's time)
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Static split of the attention passes' key tiles over a persistent grid.
+struct AttnSched {
+  int C;            // kept-row key tiles, ceil(k / 128)
+  int Q;            // query quads, ceil(m / 512)
+  int per_bh;       // key tiles of all quads of one (b, h)
+  int bh_count;
+  int ctas;
+  long long total;  // per_bh * bh_count
+  // first key tile of CTA c; CTA c takes [begin(c), begin(c + 1))
+  __host__ __device__ long long begin(int c) const { return total * c / ctas; }
+  // the CTA whose share holds key tile g
+  __host__ __device__ int cta_of(long long g) const { return (int)(((g + 1) * ctas + total - 1) / total) - 1; }
+};
+
 struct CurdkvParams {
+  CUtensorMap tm_kin;    // incoming keys [BH][m][128] bf16, boxes of 128 rows x 64 elements, 128-byte swizzle
+  CUtensorMap tm_kst;    // kept keys [BH][k][128] (row pitch cap), same boxes; unused when k = 0
+  AttnSched sched1, sched2;
+  float* colpart;        // [Q, BH, rows] per-quad column sums (= attn when Q = 1)
   const void* k_in;      // [BH, m, D] bf16
   const void* v_in;
   const void* kst;       // [BH, cap, D] bf16
@@ -94,10 +117,6 @@ struct CurdkvParams {
   int* err;
 };
 
-__device__ __forceinline__ const char* key_row(const CurdkvParams& p, int bh, int i) {
-  if (i < p.k) return static_cast<const char*>(p.kst) + ((size_t)bh * p.cap + i) * (kHeadDim * 2);
-  return static_cast<const char*>(p.k_in) + ((size_t)bh * p.m + (i - p.k)) * (kHeadDim * 2);
-}
 __device__ __forceinline__ const char* value_row(const CurdkvParams& p, int bh, int i) {
   if (i < p.k) return static_cast<const char*>(p.vst) + ((size_t)bh * p.cap + i) * (kHeadDim * 2);
   return static_cast<const char*>(p.v_in) + ((size_t)bh * p.m + (i - p.k)) * (kHeadDim * 2);
@@ -128,299 +147,450 @@ __device__ __forceinline__ void issue_tile_mma(uint32_t tmem, uint32_t a, uint32
 }
 
 // ---------------------------------------------------------------------------
-// Pipelined attention passes. Each CTA holds two fixed 128-row operand tiles
-// (256 queries in pass 1, 256 keys in pass 2) and streams the other operand
-// through a 3-stage cp.async ring; every streamed tile feeds two 128 x 128
-// MMAs. TMEM holds two buffers of two fp32 accumulators (512 columns), so
-// the MMAs of tile i+1 run while tile i is read. 512 threads: warp w reads
-// TMEM lanes 32*(w%4)..+31 (one accumulator row per thread) and, with
-// g = w/4, accumulator g/2, columns 64*(g%2)..+63.
+// Proxy-softmax attention passes: tensor cores, TMA, warp specialisation and
+// a persistent grid.
+//
+// Work unit = (b, h, query quad): up to four 128-row tiles of incoming rows
+// (512 proxy queries), held fixed in shared memory while the key tiles they
+// can see stream through a ring. Key tiles are aligned to the end of the kept
+// rows: kept tile c covers rows k - 128 (C - c) .. +127 (the first may start
+// below zero; TMA fills those rows with zeros), incoming tile u covers rows
+// k + 128 u .. +127. No tile mixes the two buffers, so each is one pair of
+// TMA boxes. The key tiles of all units are laid end to end and every CTA
+// takes an equal contiguous share: one wave of CTAs with equal work; a unit
+// may be shared by neighbouring CTAs (pass 1 then leaves one partial per CTA).
+//
+// Roles (576 threads): warps 0-15 read the accumulators (warp w: TMEM lanes
+// 32 (w % 4) .. +31, accumulator w / 4 = query tile w / 4 of the quad);
+// warp 16 issues the TMA loads; warp 17 issues the MMAs. Each query tile has
+// its own 128-column fp32 accumulator (512 TMEM columns), so the MMAs of one
+// accumulator run while the other three are read. mbarriers connect the
+// roles; every wait is bounded and a timeout stops the CTA cleanly.
 // ---------------------------------------------------------------------------
-constexpr int kPipeThreads = 512;
-constexpr int kColGroups = 4;                     // column groups of 64 over the two accumulators
-constexpr int kStages = 3;
-constexpr int kPipeSmem = (2 + kStages) * kTileBytes + 1024;
-constexpr int kMaxLseSplit = 8;
+constexpr int kQuad = 4;                          // fixed query tiles per unit
+constexpr int kSoftWarps = 16;
+constexpr int kAttnCtaThreads = (kSoftWarps + 2) * 32;
+constexpr int kMaxLseSplit = 8;                   // CTAs that may share one unit in pass 1
+constexpr int kLseStages = 3, kColStages = 2;
+constexpr int attn_smem_bytes(int stages) { return (kQuad + stages) * kTileBytes + 1024; }
 
-// cp.async of one 128-row tile (rows >= row_end are zero) by all threads.
-__device__ __forceinline__ void pipe_load_rows(const CurdkvParams& p, int bh, uint32_t tile, int row0, int row_end) {
-#pragma unroll
-  for (int q = 0; q < kTile * 16 / kPipeThreads; ++q) {
-    const int c = threadIdx.x + q * kPipeThreads;
-    const int r = c >> 4, j = c & 15;
-    const int row = row0 + r;
-    const bool ok = row < row_end;
-    const char* src = key_row(p, bh, ok ? row : 0) + j * 16;
-    tc::cp_async16(tile + tc::sw128_offset(r, j, kTile), src, ok ? 16u : 0u);
-  }
+// Key tiles seen by quad q: every kept tile and the incoming tiles up to the quad's last query.
+__host__ __device__ __forceinline__ int quad_tiles(int C, int m, int q) {
+  const int last = (m < kQuad * kTile * (q + 1) ? m : kQuad * kTile * (q + 1)) - 1;
+  return C + last / kTile + 1;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-
-// Warp-uniform bounded wait for an MMA commit; every lane returns the same answer.
-__device__ __forceinline__ bool warp_wait_mma(uint64_t* bar, uint32_t parity, int* err) {
-  bool ok = false;
-  for (int spin = 0; spin < kMbarSpin && !ok; ++spin) ok = tc::mbar_try_wait(bar, parity);
-  ok = __all_sync(0xffffffffu, ok);
-  if (!ok && (threadIdx.x & 31) == 0) raise_device_error(err, kDevWaitTimeout);
-  return ok;
-}
-
-// MMAs of one streamed tile into buffer `buf`: accumulator a = fixed tile a x streamed tile.
-// `two` = the second fixed tile holds real rows. Pass 1 puts the fixed tiles
-// on the A side (rows = queries), pass 2 too (rows = keys).
-__device__ __forceinline__ void issue_pair(uint32_t tmem, int buf, uint32_t fixed0, uint32_t streamed, bool two,
-                                           uint64_t* bar) {
-  tc::fence_after_sync();
-  issue_tile_mma(tmem + (uint32_t)(buf * 2 * kTile), fixed0, streamed);
-  if (two) issue_tile_mma(tmem + (uint32_t)(buf * 2 * kTile + kTile), fixed0 + kTileBytes, streamed);
-  tc::mma_commit(bar);
+// Key tiles of quads 0 .. q-1 (all full: quad j sees C + 4 j + 4 tiles).
+__host__ __device__ __forceinline__ int quad_prefix(int C, int q) { return q * C + 2 * q * (q + 1); }
+// Query tiles of quad q that hold at least one incoming row.
+__host__ __device__ __forceinline__ int quad_rows(int m, int q) {
+  const int left = (m - kQuad * kTile * q + kTile - 1) / kTile;
+  return left < kQuad ? left : kQuad;
 }
 
-// ---------------------------------------------------------------------------
-// Pass 1 (split over keys): for query t of the CTA's 256 and key split s,
-//   (m, s) = (max_i x_i, sum_i 2^(x_i - max)),  x_i = scale2 * q_t . k_i,
-// over the split's share of the keys i <= k + t. grid = (ceil(m/256), S, B*H).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPipeThreads, 1) curdkv_lse_kernel(const __grid_constant__ CurdkvParams p) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t bar[2];
-  __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
-  __shared__ float s_m[kColGroups][kTile], s_s[kColGroups][kTile];
-  const int t0 = blockIdx.x * 2 * kTile, split = blockIdx.y, n_split = gridDim.y, bh = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = warp >> 2, a = g >> 1, col0 = 64 * (g & 1);
-  const int row = 32 * (warp & 3) + lane;
-  const int t = t0 + a * kTile + row;                // this thread's query
-  const bool two = t0 + kTile < p.m;                 // the second query tile exists
-  const int t_last = min(p.m, t0 + 2 * kTile) - 1;
-  const int key_end = p.k + t_last + 1;
-  const int n_kt = (key_end + kTile - 1) / kTile;
-  const int per = (n_kt + n_split - 1) / n_split;
-  const int kt_begin = split * per, kt_end = min(n_kt, kt_begin + per);
-  float2* part = p.lse_part + ((size_t)bh * kMaxLseSplit + split) * p.lse_stride;
-  if (kt_begin >= kt_end) {                          // nothing to see in this split
-    if ((g & 1) == 0 && t < p.m) part[t] = make_float2(-INFINITY, 0.f);
-    return;
+// Cursor over the flattened key tiles (b, h) -> quad -> key tile.
+struct UnitCursor {
+  int bh, q, kt, tiles;
+  __device__ void init(const AttnSched& s, int m, long long g) {
+    bh = (int)(g / s.per_bh);
+    int rem = (int)(g - (long long)bh * s.per_bh);
+    q = 0;
+    while (rem >= quad_tiles(s.C, m, q)) rem -= quad_tiles(s.C, m, q++);
+    kt = rem;
+    tiles = quad_tiles(s.C, m, q);
   }
-  const int T = kt_end - kt_begin;
-  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t q_tiles = tc::smem_u32(smem), stage0 = q_tiles + 2 * kTileBytes;
-  if (tid == 0) {
-    tc::mbar_init(&bar[0], 1);
-    tc::mbar_init(&bar[1], 1);
-    s_fail = 0;
-  }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, 4 * kTile);
-  pipe_load_rows(p, bh, q_tiles, p.k + t0, p.k + p.m);                  // queries = incoming rows
-  pipe_load_rows(p, bh, q_tiles + kTileBytes, p.k + t0 + kTile, p.k + p.m);
-  cp_async_commit();
-  pipe_load_rows(p, bh, stage0, kt_begin * kTile, key_end);
-  cp_async_commit();
-  if (T > 1) pipe_load_rows(p, bh, stage0 + kTileBytes, (kt_begin + 1) * kTile, key_end);
-  cp_async_commit();
-  cp_async_wait_1();
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_base;
-  if (tid == 0) issue_pair(tmem, 0, q_tiles, stage0, two, &bar[0]);
-  const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
-  const bool active = a == 0 || two;                 // warp-uniform: this warp's accumulator exists
-  float run_max = -INFINITY, run_sum = 0.f;
-  int consumed = 0, issued = 1;
-  for (int it = 0; it < T; ++it) {
-    if (it + 2 < T) pipe_load_rows(p, bh, stage0 + ((it + 2) % kStages) * kTileBytes, (kt_begin + it + 2) * kTile, key_end);
-    cp_async_commit();
-    cp_async_wait_1();
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (s_fail) break;
-    if (it + 1 < T) {
-      if (tid == 0) issue_pair(tmem, (it + 1) & 1, q_tiles, stage0 + ((it + 1) % kStages) * kTileBytes, two,
-                               &bar[(it + 1) & 1]);
-      ++issued;
-    }
-    if (!warp_wait_mma(&bar[it & 1], (uint32_t)((it >> 1) & 1), p.err)) {
-      if (lane == 0) s_fail = 1;
-      continue;                                      // the next barrier sees s_fail
-    }
-    ++consumed;
-    tc::fence_after_sync();
-    if (active) {
-      const int i0 = (kt_begin + it) * kTile;
-      const bool full = i0 + kTile - 1 <= p.k + t0 + a * kTile;   // every key visible to every query
-      const uint32_t acc = tmem + (uint32_t)((it & 1) * 2 * kTile + a * kTile + col0) + tlane;
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(acc + c0, v);
-        if (!full) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (i0 + col0 + c0 + c > p.k + t) v[c] = -INFINITY;
-        }
-        float mx[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(v[c], v[c + 8]), fmaxf(v[c + 16], v[c + 24]));
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
-        if (mx[0] > -INFINITY) {
-          const float nm = fmaxf(run_max, mx[0] * p.scale2);
-          float sm[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int c = 0; c < 32; ++c) sm[c & 3] += ex2(fmaf(v[c], p.scale2, -nm));
-          run_sum = (run_max > -INFINITY ? run_sum * ex2(run_max - nm) : 0.f) + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
-          run_max = nm;
-        }
+  __device__ void next(const AttnSched& s, int m) {
+    if (++kt == tiles) {
+      kt = 0;
+      if (++q == s.Q) {
+        q = 0;
+        ++bh;
       }
+      tiles = quad_tiles(s.C, m, q);
     }
-    tc::fence_before_sync();
   }
-  // a failure can leave MMAs in flight: wait for them (bounded) before freeing TMEM
-  if (issued > consumed) warp_wait_mma(&bar[consumed & 1], (uint32_t)((consumed >> 1) & 1), p.err);
-  s_m[g][row] = run_max;
-  s_s[g][row] = run_sum;
-  tc::fence_before_sync();
-  __syncthreads();
-  if ((g & 1) == 0 && active && !s_fail && t < p.m) {
-    const float m0 = s_m[g][row], m1 = s_m[g + 1][row];
-    const float mm = fmaxf(m0, m1);
-    float ss = 0.f;
-    if (mm > -INFINITY)
-      ss = (m0 > -INFINITY ? s_s[g][row] * ex2(m0 - mm) : 0.f) + (m1 > -INFINITY ? s_s[g + 1][row] * ex2(m1 - mm) : 0.f);
-    part[t] = make_float2(mm, ss);
+};
+
+// Bounded wait on an mbarrier phase. Gives up early once the CTA's failure
+// flag is set; after kMbarSpin polls it sets the flag and the error word.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* fail, int* err) {
+  for (int spin = 0; spin < kMbarSpin; ++spin) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((spin & 63) == 63 && *fail) return false;
   }
-  if (warp == 0) tc::tmem_dealloc(tmem, 4 * kTile);
+  *fail = 1;
+  raise_device_error(err, kDevWaitTimeout);
+  return false;
+}
+// The same wait ignoring the failure flag: used to let copies and MMAs already
+// issued finish before the CTA releases its shared and tensor memory.
+__device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity, int* err) {
+  for (int spin = 0; spin < kMbarSpin; ++spin)
+    if (tc::mbar_try_wait(bar, parity)) return;
+  raise_device_error(err, kDevWaitTimeout);
 }
 
-// Merge the key splits: lse2[t] = log2 sum_s s_s 2^(m_s). grid = ceil(m / 256) x B*H.
-__global__ void __launch_bounds__(256) curdkv_lse_merge_kernel(const __grid_constant__ CurdkvParams p, int n_split) {
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Shared state of one attention CTA (static shared memory).
+struct AttnBars {
+  uint64_t stage_full[kLseStages], stage_empty[kLseStages];
+  uint64_t fixed_full, fixed_empty;
+  uint64_t acc_full[kQuad], acc_empty[kQuad];
+  uint32_t tmem_base;
+  int fail;
+};
+
+// The two data-movement roles, shared by both passes.
+// kColsum = false: pass 1, accumulator a = fixed query tile a x streamed keys.
+// kColsum = true:  pass 2, accumulator a = streamed keys x fixed query tile a.
+template <int kStagesT>
+__device__ void attn_producer(const CurdkvParams& p, const AttnSched& s, AttnBars& b, uint32_t fixed,
+                              uint32_t stage0, long long g0, long long g1) {
+  UnitCursor u;
+  u.init(s, p.m, g0);
+  int units = 0, issued[kStagesT];
+#pragma unroll
+  for (int i = 0; i < kStagesT; ++i) issued[i] = 0;
+  tc::tma_prefetch_desc(&p.tm_kin);
+  if (s.C > 0) tc::tma_prefetch_desc(&p.tm_kst);
+  for (long long g = g0; g < g1; ++g) {
+    const int j = (int)(g - g0);
+    if (g == g0 || u.kt == 0) {                   // a new unit: its query tiles
+      if (!wait_phase(&b.fixed_empty, (uint32_t)((units & 1) ^ 1), &b.fail, p.err)) break;
+      const int nq = quad_rows(p.m, u.q);
+      tc::mbar_arrive_expect_tx(&b.fixed_full, (uint32_t)(nq * kTileBytes));
+      for (int a = 0; a < nq; ++a)
+        for (int hf = 0; hf < 2; ++hf)
+          tc::tma_load_3d(fixed + a * kTileBytes + hf * (kTileBytes / 2), &p.tm_kin, 64 * hf,
+                          kQuad * kTile * u.q + kTile * a, u.bh, &b.fixed_full);
+      ++units;
+    }
+    const int st = j % kStagesT;
+    if (!wait_phase(&b.stage_empty[st], (uint32_t)(((j / kStagesT) & 1) ^ 1), &b.fail, p.err)) break;
+    tc::mbar_arrive_expect_tx(&b.stage_full[st], (uint32_t)kTileBytes);
+    const bool kept = u.kt < s.C;
+    const void* map = kept ? (const void*)&p.tm_kst : (const void*)&p.tm_kin;
+    const int y = kept ? p.k - kTile * (s.C - u.kt) : kTile * (u.kt - s.C);
+    for (int hf = 0; hf < 2; ++hf)
+      tc::tma_load_3d(stage0 + st * kTileBytes + hf * (kTileBytes / 2), map, 64 * hf, y, u.bh, &b.stage_full[st]);
+    ++issued[st];
+    u.next(s, p.m);
+  }
+  // every copy issued must land before the CTA may release its shared memory
+  for (int i = 0; i < kStagesT; ++i)
+    if (issued[i] > 0) drain_phase(&b.stage_full[i], (uint32_t)((issued[i] - 1) & 1), p.err);
+  if (units > 0) drain_phase(&b.fixed_full, (uint32_t)((units - 1) & 1), p.err);
+}
+
+template <int kStagesT, bool kColsum>
+__device__ void attn_mma(const CurdkvParams& p, const AttnSched& s, AttnBars& b, uint32_t tmem, uint32_t fixed,
+                         uint32_t stage0, long long g0, long long g1) {
+  UnitCursor u;
+  u.init(s, p.m, g0);
+  int units = 0, uses[kQuad] = {0, 0, 0, 0};
+  bool ok = true;
+  for (long long g = g0; g < g1 && ok; ++g) {
+    const int j = (int)(g - g0);
+    const int nq = quad_rows(p.m, u.q);
+    if (g == g0 || u.kt == 0) {
+      if (!wait_phase(&b.fixed_full, (uint32_t)(units & 1), &b.fail, p.err)) break;
+      ++units;
+    }
+    const int st = j % kStagesT;
+    if (!wait_phase(&b.stage_full[st], (uint32_t)((j / kStagesT) & 1), &b.fail, p.err)) break;
+    const uint32_t keys = stage0 + st * kTileBytes;
+    for (int a = 0; a < nq; ++a) {
+      if (!wait_phase(&b.acc_empty[a], (uint32_t)((uses[a] & 1) ^ 1), &b.fail, p.err)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t q_tile = fixed + a * kTileBytes;
+      if (kColsum) issue_tile_mma(tmem + (uint32_t)(a * kTile), keys, q_tile);
+      else issue_tile_mma(tmem + (uint32_t)(a * kTile), q_tile, keys);
+      tc::mma_commit(&b.acc_full[a]);
+      ++uses[a];
+    }
+    if (!ok) break;
+    tc::mma_commit(&b.stage_empty[st]);
+    if (u.kt == u.tiles - 1) tc::mma_commit(&b.fixed_empty);
+    u.next(s, p.m);
+  }
+  // the accumulators' last MMAs must finish before TMEM is released
+  for (int a = 0; a < kQuad; ++a)
+    if (uses[a] > 0) drain_phase(&b.acc_full[a], (uint32_t)((uses[a] - 1) & 1), p.err);
+}
+
+// Bounded, warp-uniform wait of an accumulator-reading warp.
+__device__ __forceinline__ bool warp_wait_acc(uint64_t* bar, uint32_t parity, AttnBars& b, int* err) {
+  bool ok = wait_phase(bar, parity, &b.fail, err);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// 64 accumulator columns of this thread's row (two 32-column loads, one wait).
+__device__ __forceinline__ void load64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r0[32], r1[32];
+  tc::tmem_ld32_nowait(taddr, r0);
+  tc::tmem_ld32_nowait(taddr + 32, r1);
+  tc::tmem_wait_ld32x2(r0, r1);
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    v[c] = __uint_as_float(r0[c]);
+    v[c + 32] = __uint_as_float(r1[c]);
+  }
+}
+
+// Setup shared by both passes: barriers, TMEM, this CTA's share of the tiles.
+template <int kStagesT>
+__device__ __forceinline__ void attn_setup(AttnBars& b) {
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesT; ++i) {
+      tc::mbar_init(&b.stage_full[i], 1);
+      tc::mbar_init(&b.stage_empty[i], 1);
+    }
+    tc::mbar_init(&b.fixed_full, 1);
+    tc::mbar_init(&b.fixed_empty, 1);
+    for (int a = 0; a < kQuad; ++a) {
+      tc::mbar_init(&b.acc_full[a], 1);
+      tc::mbar_init(&b.acc_empty[a], 4);         // the four warps reading accumulator a
+    }
+    b.fail = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&b.tmem_base, kQuad * kTile);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+}
+
+__device__ __forceinline__ void attn_teardown(AttnBars& b) {
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if ((threadIdx.x >> 5) == 0) tc::tmem_dealloc(b.tmem_base, kQuad * kTile);
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1: for each proxy query t, (max, sum) of 2^x over the keys i <= k + t
+// that this CTA streams, x = scale2 * q_t . k_i (base 2). A unit shared by
+// several CTAs leaves one partial per CTA (slot = CTA - first CTA of the unit).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_lse_kernel(const __grid_constant__ CurdkvParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ AttnBars b;
+  const AttnSched& s = p.sched1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t fixed = tc::smem_u32(smem), stage0 = fixed + kQuad * kTileBytes;
+  const long long g0 = s.begin(blockIdx.x), g1 = s.begin(blockIdx.x + 1);
+  attn_setup<kLseStages>(b);
+  const uint32_t tmem = b.tmem_base;
+  if (warp == kSoftWarps) {
+    if (lane == 0) attn_producer<kLseStages>(p, s, b, fixed, stage0, g0, g1);
+    __syncwarp();
+  } else if (warp == kSoftWarps + 1) {
+    if (lane == 0) attn_mma<kLseStages, false>(p, s, b, tmem, fixed, stage0, g0, g1);
+    __syncwarp();
+  } else {
+    const int a = warp >> 2, row = 32 * (warp & 3) + lane;
+    const uint32_t acc = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(a * kTile);
+    UnitCursor u;
+    u.init(s, p.m, g0);
+    int uses = 0;
+    bool dead = false;
+    float run_max = -INFINITY, run_sum = 0.f;
+    for (long long g = g0; g < g1; ++g) {
+      const int nq = quad_rows(p.m, u.q);
+      const int t = kQuad * kTile * u.q + kTile * a + row;        // this thread's query
+      if (a < nq && !dead) {
+        if (!warp_wait_acc(&b.acc_full[a], (uint32_t)(uses & 1), b, p.err)) dead = true;
+        ++uses;
+      }
+      if (a < nq && !dead) {
+        tc::fence_after_sync();
+        const bool kept = u.kt < s.C;
+        const int base = kept ? p.k - kTile * (s.C - u.kt) : p.k + kTile * (u.kt - s.C);
+        // every key of the tile is a real row visible to every query of the accumulator
+        const bool full = kept ? base >= 0 : kTile * (u.kt - s.C) + kTile - 1 <= kQuad * kTile * u.q + kTile * a;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          float v[64];
+          load64(acc + (uint32_t)(64 * hf), v);
+          if (!full) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const int i = base + 64 * hf + c;
+              if (i < 0 || i > p.k + t) v[c] = -INFINITY;
+            }
+          }
+          float mx[22];
+#pragma unroll
+          for (int c = 0; c < 21; ++c) mx[c] = fmax3(v[3 * c], v[3 * c + 1], v[3 * c + 2]);
+          mx[21] = v[63];
+#pragma unroll
+          for (int c = 0; c < 7; ++c) mx[c] = fmax3(mx[3 * c], mx[3 * c + 1], mx[3 * c + 2]);
+          mx[7] = mx[21];
+          const float m8 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+          if (m8 > -INFINITY) {
+            const float nm = fmaxf(run_max, m8 * p.scale2);
+            float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 64; ++c) sm[c & 7] += ex2(fmaf(v[c], p.scale2, -nm));
+            const float tot = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+            run_sum = run_sum * ex2(run_max - nm) + tot;         // ex2(-inf) = 0 on the first visible tile
+            run_max = nm;
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&b.acc_empty[a]);
+      }
+      if (u.kt == u.tiles - 1 || g == g1 - 1) {                   // this CTA's part of the unit ends
+        if (a < nq && !dead && t < p.m) {
+          const long long first = (long long)u.bh * s.per_bh + quad_prefix(s.C, u.q);
+          const int slot = (int)blockIdx.x - s.cta_of(first);
+          p.lse_part[((size_t)u.bh * kMaxLseSplit + slot) * p.lse_stride + t] = make_float2(run_max, run_sum);
+        }
+        run_max = -INFINITY;
+        run_sum = 0.f;
+      }
+      u.next(s, p.m);
+    }
+  }
+  attn_teardown(b);
+}
+
+// Merge the per-CTA partials: lse2[t] = log2 sum_s s_s 2^(m_s). grid = (ceil(m / 256), B*H).
+__global__ void __launch_bounds__(256) curdkv_lse_merge_kernel(const __grid_constant__ CurdkvParams p) {
+  const AttnSched& s = p.sched1;
   const int bh = blockIdx.y, t = blockIdx.x * 256 + threadIdx.x;
   if (t >= p.m) return;
+  const int q = t / (kQuad * kTile);
+  const long long first = (long long)bh * s.per_bh + quad_prefix(s.C, q);
+  const int n_seg = s.cta_of(first + quad_tiles(s.C, p.m, q) - 1) - s.cta_of(first) + 1;
   const float2* part = p.lse_part + (size_t)bh * kMaxLseSplit * p.lse_stride + t;
   float mm = -INFINITY;
-  for (int s = 0; s < n_split; ++s) mm = fmaxf(mm, part[(size_t)s * p.lse_stride].x);
+  for (int i = 0; i < n_seg; ++i) mm = fmaxf(mm, part[(size_t)i * p.lse_stride].x);
   float ss = 0.f;
-  for (int s = 0; s < n_split; ++s) {
-    const float2 v = part[(size_t)s * p.lse_stride];
+  for (int i = 0; i < n_seg; ++i) {
+    const float2 v = part[(size_t)i * p.lse_stride];
     if (v.x > -INFINITY) ss += v.y * ex2(v.x - mm);
   }
   p.lse[(size_t)bh * p.lse_stride + t] = mm + log2f(ss);
 }
 
 // ---------------------------------------------------------------------------
-// Pass 2: attn[i] = sum_{t : k+t >= i} 2^(scale2 * q_t . k_i - lse2[t]).
-// The CTA's 256 keys are fixed (MMA operand A); query tiles stream through
-// the ring with their lse2 values. grid = (ceil(n / 256), B*H).
+// Pass 2: for each key i and query quad q,
+//   part_q[i] = sum over the quad's queries t with i <= k + t of 2^(x - lse2[t]).
+// Accumulator a holds keys x query tile a; the four warps of one TMEM lane
+// quarter each sum one query tile and combine their sums in shared memory
+// in a fixed order. With one quad the sums are the column sums themselves.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPipeThreads, 1) curdkv_colsum_kernel(const __grid_constant__ CurdkvParams p) {
+__global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t bar[2];
-  __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
-  __shared__ __align__(16) float s_lse[kStages][kTile];
-  __shared__ float s_acc[kColGroups][kTile];
-  const int i0 = blockIdx.x * 2 * kTile, bh = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = warp >> 2, a = g >> 1, col0 = 64 * (g & 1);
-  const int row = 32 * (warp & 3) + lane;
-  const int i = i0 + a * kTile + row;              // this thread's key
-  const int key_end = min(p.n, i0 + 2 * kTile);
-  const bool two = i0 + kTile < p.n;               // the second key tile exists
-  const int t_first = max(0, i0 - p.k);            // first query that sees a key of the CTA
-  const int tq0 = (t_first / kTile) * kTile;
-  const int T = (p.m - tq0 + kTile - 1) / kTile;   // >= 1: the last key is seen by the last query
+  __shared__ AttnBars b;
+  __shared__ __align__(16) float s_lse[2][kQuad * kTile];
+  __shared__ float s_part[2][kQuad][kTile];
+  const AttnSched& s = p.sched2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t k_tiles = tc::smem_u32(smem), stage0 = k_tiles + 2 * kTileBytes;
-  const float* lse = p.lse + (size_t)bh * p.lse_stride;
-  auto load_stage = [&](int it) {
-    const int tq = tq0 + it * kTile, st = it % kStages;
-    pipe_load_rows(p, bh, stage0 + st * kTileBytes, p.k + tq, p.k + p.m);
-    if (tid < kTile / 4) {
-      const bool ok = tq + 4 * tid < p.m;          // values past m are never read
-      tc::cp_async16(tc::smem_u32(&s_lse[st][4 * tid]), lse + (ok ? tq + 4 * tid : 0), ok ? 16u : 0u);
-    }
-  };
-  if (tid == 0) {
-    tc::mbar_init(&bar[0], 1);
-    tc::mbar_init(&bar[1], 1);
-    s_fail = 0;
-  }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, 4 * kTile);
-  pipe_load_rows(p, bh, k_tiles, i0, key_end);
-  pipe_load_rows(p, bh, k_tiles + kTileBytes, i0 + kTile, key_end);
-  cp_async_commit();
-  load_stage(0);
-  cp_async_commit();
-  if (T > 1) load_stage(1);
-  cp_async_commit();
-  cp_async_wait_1();
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_base;
-  if (tid == 0) issue_pair(tmem, 0, k_tiles, stage0, two, &bar[0]);
-  const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
-  const bool active = a == 0 || two;               // warp-uniform: this warp's accumulator exists
-  const int key_base = i0 + a * kTile;             // first key of this warp's accumulator
-  float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-  int consumed = 0, issued = 1;
-  for (int it = 0; it < T; ++it) {
-    if (it + 2 < T) load_stage(it + 2);
-    cp_async_commit();
-    cp_async_wait_1();
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (s_fail) break;
-    if (it + 1 < T) {
-      if (tid == 0) issue_pair(tmem, (it + 1) & 1, k_tiles, stage0 + ((it + 1) % kStages) * kTileBytes, two,
-                               &bar[(it + 1) & 1]);
-      ++issued;
-    }
-    if (!warp_wait_mma(&bar[it & 1], (uint32_t)((it >> 1) & 1), p.err)) {
-      if (lane == 0) s_fail = 1;
-      continue;
-    }
-    ++consumed;
-    tc::fence_after_sync();
-    if (active) {
-      const int tq = tq0 + it * kTile;
-      const float* l = s_lse[it % kStages] + col0;
-      // every query of the tile exists and sees every key of the accumulator
-      const bool full = tq + kTile <= p.m && key_base + kTile - 1 <= p.k + tq;
-      const uint32_t acc = tmem + (uint32_t)((it & 1) * 2 * kTile + a * kTile + col0) + tlane;
+  const uint32_t fixed = tc::smem_u32(smem), stage0 = fixed + kQuad * kTileBytes;
+  const long long g0 = s.begin(blockIdx.x), g1 = s.begin(blockIdx.x + 1);
+  attn_setup<kColStages>(b);
+  const uint32_t tmem = b.tmem_base;
+  if (warp == kSoftWarps) {
+    if (lane == 0) attn_producer<kColStages>(p, s, b, fixed, stage0, g0, g1);
+    __syncwarp();
+  } else if (warp == kSoftWarps + 1) {
+    if (lane == 0) attn_mma<kColStages, true>(p, s, b, tmem, fixed, stage0, g0, g1);
+    __syncwarp();
+  } else {
+    const int a = warp >> 2, row = 32 * (warp & 3) + lane, tid = threadIdx.x;
+    const uint32_t acc = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(a * kTile);
+    const float* lse = p.lse;
+    UnitCursor u;
+    u.init(s, p.m, g0);
+    int uses = 0, units = 0;
+    bool dead = false;
+    for (long long g = g0; g < g1; ++g) {
+      const int j = (int)(g - g0);
+      const int nq = quad_rows(p.m, u.q);
+      if (g == g0 || u.kt == 0) {                  // the quad's lse2, +inf past the last query
+        const int t = kQuad * kTile * u.q + tid;
+        s_lse[units & 1][tid] = t < p.m ? lse[(size_t)u.bh * p.lse_stride + t] : INFINITY;
+        ++units;
+        tc::named_sync(1, kSoftWarps * 32);
+      }
+      const float* l = s_lse[(units - 1) & 1] + kTile * a;
+      float part = 0.f;
+      if (a < nq && !dead) {
+        if (!warp_wait_acc(&b.acc_full[a], (uint32_t)(uses & 1), b, p.err)) dead = true;
+        ++uses;
+      }
+      const bool kept = u.kt < s.C;
+      const int base = kept ? p.k - kTile * (s.C - u.kt) : p.k + kTile * (u.kt - s.C);
+      const int i = base + row;                    // this thread's key
+      if (a < nq && !dead) {
+        tc::fence_after_sync();
+        const int tq = kQuad * kTile * u.q + kTile * a;            // first query of the accumulator
+        const bool full = kept || kTile * (u.kt - s.C) + kTile - 1 <= tq;
+        float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          float v[64];
+          load64(acc + (uint32_t)(64 * hf), v);
+          const float* lh = l + 64 * hf;
+          if (full) {
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(acc + c0, v);
-        if (full) {
+            for (int c = 0; c < 64; c += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lh + c);
+              sm[0] += ex2(fmaf(v[c], p.scale2, -l4.x));
+              sm[1] += ex2(fmaf(v[c + 1], p.scale2, -l4.y));
+              sm[2] += ex2(fmaf(v[c + 2], p.scale2, -l4.z));
+              sm[3] += ex2(fmaf(v[c + 3], p.scale2, -l4.w));
+            }
+          } else {
+            const int first_t = i - p.k - tq - 64 * hf;              // columns c >= first_t see key i
 #pragma unroll
-          for (int c = 0; c < 32; ++c) acc4[c & 3] += ex2(fmaf(v[c], p.scale2, -l[c0 + c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int tt = tq + col0 + c0 + c;
-            if (tt < p.m && i <= p.k + tt) acc4[c & 3] += ex2(fmaf(v[c], p.scale2, -l[c0 + c]));
+            for (int c = 0; c < 64; ++c)
+              if (c >= first_t) sm[c & 3] += ex2(fmaf(v[c], p.scale2, -lh[c]));
           }
         }
+        part = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&b.acc_empty[a]);
       }
+      s_part[j & 1][a][row] = part;
+      tc::named_sync(1, kSoftWarps * 32);
+      if (a == 0 && !b.fail && i >= 0 && i < p.n) {
+        const float* sp = &s_part[j & 1][0][row];
+        p.colpart[((size_t)u.q * s.bh_count + u.bh) * p.rows + i] =
+            (sp[0] + sp[kTile]) + (sp[2 * kTile] + sp[3 * kTile]);
+      }
+      u.next(s, p.m);
     }
-    tc::fence_before_sync();
   }
-  if (issued > consumed) warp_wait_mma(&bar[consumed & 1], (uint32_t)((consumed >> 1) & 1), p.err);
-  s_acc[g][row] = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-  tc::fence_before_sync();
-  __syncthreads();
-  if ((g & 1) == 0 && active && !s_fail && i < key_end) p.attn[(size_t)bh * p.rows + i] = s_acc[g][row] + s_acc[g + 1][row];
-  if (warp == 0) tc::tmem_dealloc(tmem, 4 * kTile);
+  attn_teardown(b);
+}
+
+// attn[i] = sum of the quads' partial column sums, over the quads whose key
+// tiles include row i. grid = (ceil(n / 256), B*H); only launched with two
+// or more quads.
+__global__ void __launch_bounds__(256) curdkv_colsum_merge_kernel(const __grid_constant__ CurdkvParams p) {
+  const AttnSched& s = p.sched2;
+  const int bh = blockIdx.y, i = blockIdx.x * 256 + threadIdx.x;
+  if (i >= p.n) return;
+  float sum = 0.f;
+  for (int q = 0; q < s.Q; ++q) {
+    if (i >= p.k && (i - p.k) / kTile > quad_tiles(s.C, p.m, q) - s.C - 1) continue;   // not seen by quad q
+    sum += p.colpart[((size_t)q * s.bh_count + bh) * p.rows + i];
+  }
+  p.attn[(size_t)bh * p.rows + i] = sum;
 }
 
 // ---------------------------------------------------------------------------
@@ -1059,6 +1229,52 @@ __global__ void __launch_bounds__(256) curdkv_append_kernel(const __grid_constan
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// Map of `rows` bf16 rows of 128 elements per (b, h), planes `pitch` rows
+// apart; boxes of 64 elements x 128 rows land in the K-major 128-byte-swizzled
+// tile layout (one box per 64-element half).
+bool encode_rows(CUtensorMap* tm, const void* base, int rows, int pitch, int bh) {
+  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows, (cuuint64_t)bh};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)pitch * kHeadDim * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_tiled()(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Equal contiguous shares of the key tiles for at most `sm_count` CTAs. With
+// `bounded_split`, every share holds at least a sixth of the largest unit, so
+// a unit spans at most 7 CTAs (the pass-1 partial slots).
+AttnSched make_sched(int k, int m, int bh, int sm_count, bool bounded_split) {
+  AttnSched s;
+  s.C = (k + kTile - 1) / kTile;
+  s.Q = (m + kQuad * kTile - 1) / (kQuad * kTile);
+  const int largest = quad_tiles(s.C, m, s.Q - 1);
+  s.per_bh = quad_prefix(s.C, s.Q - 1) + largest;
+  s.bh_count = bh;
+  s.total = (long long)s.per_bh * bh;
+  long long ctas = std::max(sm_count, 1);
+  if (bounded_split) ctas = std::min(ctas, std::max(1LL, s.total / ((largest + 5) / 6)));
+  s.ctas = (int)std::min(ctas, s.total);
+  return s;
+}
+
 }  // namespace
 
 void curdkv_layout(evict_handle* h, size_t* off, char* base) {
@@ -1077,6 +1293,8 @@ void curdkv_layout(evict_handle* h, size_t* off, char* base) {
   st.lse = reinterpret_cast<float*>(take(bh * st.lse_stride * 4));
   st.lse_part = reinterpret_cast<float2*>(take(bh * kMaxLseSplit * st.lse_stride * sizeof(float2)));
   st.attn = reinterpret_cast<float*>(take(bh * st.rows * 4));
+  st.quads = (h->cfg.max_block + kQuad * kTile - 1) / (kQuad * kTile);
+  st.colpart = st.quads > 1 ? reinterpret_cast<float*>(take((size_t)st.quads * bh * st.rows * 4)) : nullptr;
   st.lev = reinterpret_cast<float*>(take(bh * st.rows * 4));
   st.gram_part = reinterpret_cast<float*>(take(bh * st.splits * kHeadDim * kHeadDim * 4));
   st.evec = reinterpret_cast<float*>(take(bh * kCurdkvMaxRank * kHeadDim * 4));
@@ -1091,12 +1309,13 @@ void curdkv_release(evict_handle* h) {
 int curdkv_prepare(evict_handle* h) {
   cudaError_t e;
   int dev = 0;
+  if (!encode_tiled()) return fail(EVICT_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
   if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&h->curdkv->sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(curdkv_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmem)) !=
-          cudaSuccess ||
-      (e = cudaFuncSetAttribute(curdkv_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmem)) !=
-          cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn_smem_bytes(kLseStages))) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn_smem_bytes(kColStages))) != cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramTcSmem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_leverage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLevSmem)) !=
@@ -1145,26 +1364,34 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   const cudaStream_t sm = h->stream;
   cudaError_t e;
   const int k_tiles = (n + kTile - 1) / kTile;
-  // key splits for pass 1: enough CTAs to fill the GPU a few times over,
-  // each split keeping at least 4 key tiles
-  const int q_pairs = (m + 2 * kTile - 1) / (2 * kTile), k_pairs = (n + 2 * kTile - 1) / (2 * kTile);
-  int n_split = (4 * std::max(st.sm_count, 1) + q_pairs * bh - 1) / (q_pairs * bh);
-  n_split = std::max(1, std::min({n_split, kMaxLseSplit, std::max(1, k_tiles / 4)}));
+  // attention passes: TMA maps of the incoming and kept keys, tile shares
+  if (!encode_rows(&p.tm_kin, k, m, m, bh) || (p.k > 0 && !encode_rows(&p.tm_kst, h->kst, p.k, h->cap, bh)))
+    return fail(EVICT_EINVAL, "cannot describe the key buffers for TMA (k must be 16-byte aligned)");
+  p.sched1 = make_sched(p.k, m, bh, st.sm_count, true);
+  p.sched2 = make_sched(p.k, m, bh, st.sm_count, false);
+  p.colpart = p.sched2.Q > 1 ? st.colpart : st.attn;
   e = timed_launch(h, kKidCurdkvLse, [&] {
-    curdkv_lse_kernel<<<dim3(q_pairs, n_split, bh), kPipeThreads, kPipeSmem, sm>>>(p);
+    curdkv_lse_kernel<<<p.sched1.ctas, kAttnCtaThreads, attn_smem_bytes(kLseStages), sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention pass 1 launch");
   e = timed_launch(h, kKidCurdkvLseMerge, [&] {
-    curdkv_lse_merge_kernel<<<dim3((m + 255) / 256, bh), 256, 0, sm>>>(p, n_split);
+    curdkv_lse_merge_kernel<<<dim3((m + 255) / 256, bh), 256, 0, sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention merge launch");
   e = timed_launch(h, kKidCurdkvColsum, [&] {
-    curdkv_colsum_kernel<<<dim3(k_pairs, bh), kPipeThreads, kPipeSmem, sm>>>(p);
+    curdkv_colsum_kernel<<<p.sched2.ctas, kAttnCtaThreads, attn_smem_bytes(kColStages), sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention pass 2 launch");
+  if (p.sched2.Q > 1) {
+    e = timed_launch(h, kKidCurdkvColsumMerge, [&] {
+      curdkv_colsum_merge_kernel<<<dim3((n + 255) / 256, bh), 256, 0, sm>>>(p);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "CurDKV column-sum merge launch");
+  }
   e = timed_launch(h, kKidCurdkvGram, [&] {
     curdkv_gram_kernel<<<dim3((n + kGramRows - 1) / kGramRows, bh), kAttnThreads, kGramTcSmem, sm>>>(p);
     return cudaGetLastError();

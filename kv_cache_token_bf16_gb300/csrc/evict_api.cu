@@ -41,7 +41,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 const char* const kKernelNames[kKidCount] = {
     "score", "score_append", "select", "compact", "calib_gram", "calib_eig",
-    "curdkv_lse", "curdkv_lse_merge", "curdkv_colsum", "curdkv_gram", "curdkv_eig", "curdkv_leverage",
+    "curdkv_lse", "curdkv_lse_merge", "curdkv_colsum", "curdkv_colsum_merge", "curdkv_gram", "curdkv_eig", "curdkv_leverage",
 };
 
 cudaEvent_t take_event(evict_handle* h) {
@@ -239,11 +239,16 @@ int run_intrinsic(evict_handle* const* hs, int n_layers, const void* const* k, c
   return EVICT_OK;
 }
 
-int check_update_args(const evict_handle* h, const void* k, const void* v, int m) {
+// `device`: k, v (and pos) are read by the kernels directly, so they must be
+// aligned for 16-byte vector and TMA loads (4 bytes for positions).
+int check_update_args(const evict_handle* h, const void* k, const void* v, const int32_t* pos, int m, bool device) {
   if (!h) return fail(EVICT_EINVAL, "handle is NULL");
   if (m < 0) return fail(EVICT_EINVAL, "m must be >= 0 (got %d)", m);
   if (m > h->cfg.max_block) return fail(EVICT_EINVAL, "m = %d exceeds max_block = %d", m, h->cfg.max_block);
   if (m > 0 && (!k || !v)) return fail(EVICT_EINVAL, "k and v must not be NULL");
+  if (device && ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15))
+    return fail(EVICT_EINVAL, "k and v must be 16-byte aligned");
+  if (device && (reinterpret_cast<uintptr_t>(pos) & 3)) return fail(EVICT_EINVAL, "pos must be 4-byte aligned");
   return EVICT_OK;
 }
 
@@ -312,7 +317,7 @@ int evict_init(const evict_config* cfg, evict_handle** out) {
 
 int evict_update_and_fetch(evict_handle* h, const void* k, const void* v, const int32_t* pos, int m,
                            evict_view* out) {
-  int rc = check_update_args(h, k, v, m);
+  int rc = check_update_args(h, k, v, pos, m, true);
   if (rc) return rc;
   if (m > 0) {
     if (h->cfg.method == EVICT_CURDKV) {
@@ -332,7 +337,7 @@ int evict_update_and_fetch_group(evict_handle* const* hs, int n_layers, const vo
     return fail(EVICT_EINVAL, "need 1..%d handles (got %d)", kMaxGroup, n_layers);
   if (!k || !v) return fail(EVICT_EINVAL, "k and v arrays must not be NULL");
   for (int l = 0; l < n_layers; ++l) {
-    int rc = check_update_args(hs[l], k[l], v[l], m);
+    int rc = check_update_args(hs[l], k[l], v[l], pos ? pos[l] : nullptr, m, true);
     if (rc) return rc;
     if (l > 0 && !same_shape(hs[0], hs[l]))
       return fail(EVICT_EINVAL, "handle %d differs from handle 0 in shape, state or stream", l);
@@ -351,7 +356,7 @@ int evict_update_and_fetch_group(evict_handle* const* hs, int n_layers, const vo
 
 int evict_update_and_fetch_host(evict_handle* h, const void* k_host, const void* v_host, const int32_t* pos_host,
                                 int m, evict_view* out) {
-  int rc = check_update_args(h, k_host, v_host, m);
+  int rc = check_update_args(h, k_host, v_host, pos_host, m, false);
   if (rc) return rc;
   if (m > 0) {
     const size_t bytes = (size_t)h->cfg.batch * h->cfg.n_kv_heads * m * kHeadDim * h->elem;

@@ -115,7 +115,7 @@ def _run_block(B, H, budget, k_old, v_old, cum_old, k_new, v_new, n_sink=4, rece
 
 
 @pytest.mark.parametrize("k0,m,budget", [(0, 300, 64), (0, 129, 200), (500, 257, 128), (1000, 1, 64),
-                                         (127, 128, 100)])
+                                         (127, 128, 100), (0, 513, 100), (300, 1100, 256), (129, 640, 700)])
 def test_planted_spectrum_block(k0, m, budget):
     B, H = 1, 2
     n = k0 + m
@@ -223,3 +223,27 @@ def test_two_runs_are_bit_identical():
         outs.append([to_bits(t).copy() for t in view] + list(_gpu_scores(gpu, B, H)))
     for a, b in zip(*outs):
         assert a.tobytes() == b.tobytes()
+
+
+def test_units_shared_by_several_ctas():
+    """Many (b, h) units with long kept prefixes: the attention passes split
+    units across CTAs (several pass-1 partials per query) and, with m > 512,
+    across query quads (merged column sums)."""
+    B, H, k0, m, budget = 2, 4, 3000, 600, 1024
+    n = k0 + m
+    k_all = synth.clustered_keys(11, B, H, n, spread=0.5)
+    v_all = synth.planted_spectrum_values(12, B, H, n)
+    cum_old = synth.rng(13).uniform(0, 0.01, (B, H, k0))
+    _run_block(B, H, budget, k_all[:, :, :k0], v_all[:, :, :k0], cum_old, k_all[:, :, k0:], v_all[:, :, k0:],
+               units={(0, 0), (1, 3)})
+
+
+def test_misaligned_inputs_are_rejected():
+    from kv_cache_token_bf16_gb300 import binding
+    B, H, m = 1, 2, 16
+    cache = _gpu_cache(B, H, budget=64, max_block=m)
+    buf = torch.zeros((B * H * m * 128 + 8,), dtype=torch.bfloat16, device="cuda")
+    k_ok = buf.data_ptr()
+    with pytest.raises(binding.EvictError, match="16-byte aligned"):
+        binding.evict_update_and_fetch(cache.handle, k_ok + 2, k_ok, None, m)
+    assert binding.evict_stats(cache.handle)["offset"] == 0
