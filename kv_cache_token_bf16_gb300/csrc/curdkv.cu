@@ -37,6 +37,7 @@
 #include <cfloat>
 #include <cmath>
 #include <cstring>
+#include <type_traits>
 
 #include "api_internal.h"
 #include "common.cuh"
@@ -53,11 +54,10 @@ struct CurdkvState {
   int sm_count = 0;
   float* attn = nullptr;       // [BH, rows]        column sums
   float* lev = nullptr;        // [BH, rows]        leverage of the last call
-  float* gram_part = nullptr;  // [BH, splits, 128*128]
+  float* gram = nullptr;       // [BH, 128*128]
   float* evec = nullptr;       // [BH, kCurdkvMaxRank, 128]
   float* inv_e = nullptr;      // [BH]
   int rows = 0;                // cap + max_block
-  int splits = 0;              // gram partials per (b, h)
   int last_n = 0;              // rows of the last update
   float* colpart = nullptr;    // [quads, BH, rows] per-quad column sums (blocks > 512 rows)
   int quads = 0;               // ceil(max_block / 512)
@@ -66,10 +66,8 @@ struct CurdkvState {
 namespace {
 
 constexpr int kTile = 128;                  // rows of a query or key tile
-constexpr int kAttnThreads = 128;           // 4 warps: one TMEM lane per thread
 constexpr int kTileBytes = kTile * kHeadDim * 2;
-constexpr int kGramRows = 2048;             // rows per Gram partial
-constexpr int kEigThreads = 1024;
+constexpr int kEigThreads = 128;
 constexpr int kMbarSpin = 1 << 22;          // bounded MMA wait (well above a tile's time)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -90,6 +88,8 @@ struct AttnSched {
 struct CurdkvParams {
   CUtensorMap tm_kin;    // incoming keys [BH][m][128] bf16, boxes of 128 rows x 64 elements, 128-byte swizzle
   CUtensorMap tm_kst;    // kept keys [BH][k][128] (row pitch cap), same boxes; unused when k = 0
+  CUtensorMap tm_vin;    // incoming values, as tm_kin
+  CUtensorMap tm_vst;    // kept values, as tm_kst
   AttnSched sched1, sched2;
   float* colpart;        // [Q, BH, rows] per-quad column sums (= attn when Q = 1)
   const void* k_in;      // [BH, m, D] bf16
@@ -97,6 +97,7 @@ struct CurdkvParams {
   const void* kst;       // [BH, cap, D] bf16
   const void* vst;
   int k, m, n, cap, heads, rank;
+  int units;             // B * H
   float scale2;          // log2(e) / sqrt(D)
   float* lse;
   float2* lse_part;       // [BH, kMaxLseSplit, lse_stride] per-split (max, sum)
@@ -104,8 +105,8 @@ struct CurdkvParams {
   float* attn;
   float* lev;
   int rows;
-  float* gram_part;
-  int splits;
+  float* gram;            // [BH, 128, 128] G of the call
+  int gram_cluster;       // CTAs per (b, h) in the Gram kernel
   float* evec;
   float* inv_e;
   float* score_st;
@@ -117,10 +118,6 @@ struct CurdkvParams {
   int* err;
 };
 
-__device__ __forceinline__ const char* value_row(const CurdkvParams& p, int bh, int i) {
-  if (i < p.k) return static_cast<const char*>(p.vst) + ((size_t)bh * p.cap + i) * (kHeadDim * 2);
-  return static_cast<const char*>(p.v_in) + ((size_t)bh * p.m + (i - p.k)) * (kHeadDim * 2);
-}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -128,13 +125,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Wait for an MMA commit (bounded); returns false on timeout.
-__device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity, int* err) {
-  for (int spin = 0; spin < kMbarSpin; ++spin)
-    if (tc::mbar_try_wait(bar, parity)) return true;
-  raise_device_error(err, kDevWaitTimeout);
-  return false;
-}
 
 // 8 MMAs (K = 128 in steps of 16): D[128 x 128] = A[128 x 128] * B[128 x 128]^T.
 __device__ __forceinline__ void issue_tile_mma(uint32_t tmem, uint32_t a, uint32_t b) {
@@ -594,32 +584,54 @@ __global__ void __launch_bounds__(256) curdkv_colsum_merge_kernel(const __grid_c
 }
 
 // ---------------------------------------------------------------------------
-// Partial Gram of the weighted values on the tensor cores:
-//   G_part = sum over the split's rows i of a_i^2 v_i v_i^T
-//          = V^T (a^2 V)_hi + V^T (a^2 V)_lo,
-// V exact in bf16 and a_i^2 v_i split into two bf16 terms (hi + lo carries
-// ~16 significant bits; the dropped lo*lo-free remainder is below 2^-17 of
-// each term). The MMA contracts over tokens, so each 128-token tile is
-// transposed on the way into shared memory: a thread loads 8 tokens x 8
-// features (eight 16-byte rows) and rearranges them with byte permutes into
-// 8 features x 8 tokens. grid = (ceil(n / 2048), B*H), block = 128; the next
-// tile's loads overlap the running MMAs.
+// Gram of the weighted values on the tensor cores: G = sum_i a_i^2 v_i v_i^T.
+//
+// A cluster of S CTAs per (b, h). The unit's value rows are cut into 128-row
+// tiles (kept rows from row 0, then incoming rows from row k) and CTA c of the
+// cluster takes a contiguous share of them. TMA streams each tile in its
+// natural layout (tokens x features), which makes tokens the contraction
+// dimension and features the M and N dimensions: both MMA operands are
+// MN-major, so nothing is transposed. A = the value tile (exact in bf16);
+// B = a^2 v split into bf16 hi + lo (~16 significant bits; the remainder is
+// below 2^-17 of each term), two MMAs per 16-token step, fp32 accumulation
+// in TMEM. The cluster then sums its S partials through distributed shared
+// memory in a fixed order (CTA c writes rows [c R, (c+1) R) of G), so the
+// result does not depend on timing.
+//
+// Roles (320 threads): warp 0 issues the TMA loads, warp 1 the MMAs, warps
+// 2-9 write the hi / lo tiles (packed fp32x2 arithmetic) and read the
+// accumulator. Rows past the valid range of a tile are zero (TMA fill), so
+// they add nothing.
 // ---------------------------------------------------------------------------
-constexpr int kGramTcSmem = 3 * kTileBytes + 1024;
+constexpr int kGramVStages = 3, kGramHStages = 2;
+constexpr int kGramConvWarps = 8;
+constexpr int kGramThreads = (2 + kGramConvWarps) * 32;
+constexpr int kGramMaxCluster = 8;
+constexpr int kGramRedPitch = kHeadDim + 4;         // floats per row of the reduction buffer
+constexpr int kGramSmem = (kGramVStages + 2 * kGramHStages) * kTileBytes + 1024;
+static_assert(kHeadDim * kGramRedPitch * 4 <= kGramVStages * kTileBytes, "reduction buffer fits the value ring");
 
-// 8 x 8 transpose of bf16 values: in[t] holds 8 features of token t, out[f]
-// holds 8 tokens of feature f.
-__device__ __forceinline__ void transpose8x8(const uint4 (&in)[8], uint4 (&out)[8]) {
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(in);   // w[4*t + k]: features 2k, 2k+1 of token t
-#pragma unroll
-  for (int f = 0; f < 8; ++f) {
-    const uint32_t sel = (f & 1) ? 0x7632u : 0x5410u;
-    const int k = f >> 1;
-    out[f].x = __byte_perm(w[4 * 0 + k], w[4 * 1 + k], sel);
-    out[f].y = __byte_perm(w[4 * 2 + k], w[4 * 3 + k], sel);
-    out[f].z = __byte_perm(w[4 * 4 + k], w[4 * 5 + k], sel);
-    out[f].w = __byte_perm(w[4 * 6 + k], w[4 * 7 + k], sel);
-  }
+struct GramBars {
+  uint64_t v_full[kGramVStages], v_empty[kGramVStages];
+  uint64_t h_full[kGramHStages], h_empty[kGramHStages];
+  uint64_t done;
+  uint32_t tmem_base;
+  int fail;
+};
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+// Packed fp32 pairs (one instruction for two lanes of arithmetic), round to nearest.
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
@@ -627,164 +639,221 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-__global__ void __launch_bounds__(kAttnThreads) curdkv_gram_kernel(const __grid_constant__ CurdkvParams p) {
+__global__ void __launch_bounds__(kGramThreads, 1) curdkv_gram_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t bar;
-  __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
-  const int split = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+  __shared__ GramBars b;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.gram_cluster;
+  const int rank = (int)tc::cluster_rank();
+  const int bh = blockIdx.x / S;
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t a_tile = tc::smem_u32(smem), bhi_tile = a_tile + kTileBytes, blo_tile = bhi_tile + kTileBytes;
-  const int r_begin = split * kGramRows, r_end = min(p.n, r_begin + kGramRows);
-  const float* attn = p.attn + (size_t)bh * p.rows;
+  const uint32_t vring = tc::smem_u32(smem);
+  const uint32_t hring = vring + kGramVStages * kTileBytes;   // stage s: hi at 2s, lo at 2s+1
+  const int Ck = (p.k + kTile - 1) / kTile, Cm = (p.m + kTile - 1) / kTile;
+  const int T = Ck + Cm;
+  const int t0 = (int)((long long)T * rank / S), t1 = (int)((long long)T * (rank + 1) / S);
   if (tid == 0) {
-    tc::mbar_init(&bar, 1);
-    s_fail = 0;
+    for (int i = 0; i < kGramVStages; ++i) {
+      tc::mbar_init(&b.v_full[i], 1);
+      tc::mbar_init(&b.v_empty[i], 1);
+    }
+    for (int i = 0; i < kGramHStages; ++i) {
+      tc::mbar_init(&b.h_full[i], kGramConvWarps);     // one arrival per converting warp
+      tc::mbar_init(&b.h_empty[i], 1);
+    }
+    tc::mbar_init(&b.done, 1);
+    b.fail = 0;
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, kTile);
+  if (warp == 2) tc::tmem_alloc(&b.tmem_base, kTile);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = tmem_base;
+  const uint32_t tmem = b.tmem_base;
 
-  // thread -> two 8x8 blocks of the tile: token block tb, feature blocks fb and fb + 8
-  const int tb = tid & 15, fb0 = tid >> 4;
-  uint4 raw[2][8];
-  float asq[8];
-  auto load_tile = [&](int t0) {
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int row = t0 + 8 * tb + t;
-      const bool ok = row < r_end;
-      const uint4* src = reinterpret_cast<const uint4*>(value_row(p, bh, ok ? row : r_begin));
-      raw[0][t] = ok ? __ldg(src + fb0) : make_uint4(0, 0, 0, 0);
-      raw[1][t] = ok ? __ldg(src + fb0 + 8) : make_uint4(0, 0, 0, 0);
-      const float a = ok ? attn[row] : 0.f;
-      asq[t] = a * a;
+  if (warp == 0) {
+    if (lane == 0 && t1 > t0) {                         // TMA producer
+      tc::tma_prefetch_desc(&p.tm_vin);
+      if (Ck > 0) tc::tma_prefetch_desc(&p.tm_vst);
+      int issued[kGramVStages] = {0, 0, 0};
+      for (int i = t0; i < t1; ++i) {
+        const int j = i - t0, st = j % kGramVStages;
+        if (!wait_phase(&b.v_empty[st], (uint32_t)(((j / kGramVStages) & 1) ^ 1), &b.fail, p.err)) break;
+        tc::mbar_arrive_expect_tx(&b.v_full[st], (uint32_t)kTileBytes);
+        const bool kept = i < Ck;
+        const void* map = kept ? (const void*)&p.tm_vst : (const void*)&p.tm_vin;
+        const int y = kept ? kTile * i : kTile * (i - Ck);
+        for (int hf = 0; hf < 2; ++hf)
+          tc::tma_load_3d(vring + st * kTileBytes + hf * (kTileBytes / 2), map, 64 * hf, y, bh, &b.v_full[st]);
+        ++issued[st];
+      }
+      for (int i = 0; i < kGramVStages; ++i)
+        if (issued[i] > 0) drain_phase(&b.v_full[i], (uint32_t)((issued[i] - 1) & 1), p.err);
     }
-  };
-  uint32_t parity = 0;
-  int pending = 0;                                          // commits not yet waited for
-  load_tile(r_begin);
-  for (int t0 = r_begin; t0 < r_end; t0 += kTile) {
-    if (pending) {                                          // smem tiles are free once the last MMAs finished
-      if (!wait_mma(&bar, parity, p.err)) s_fail = 1;
-      else pending = 0;
-      parity ^= 1u;
-      tc::fence_after_sync();
-    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && t1 > t0) {                         // MMA issuer
+      constexpr uint32_t idesc = tc::idesc_bf16_f32_mn(kTile, kTile);
+      for (int i = t0; i < t1; ++i) {
+        const int j = i - t0, vs = j % kGramVStages, hs = j % kGramHStages;
+        if (!wait_phase(&b.v_full[vs], (uint32_t)((j / kGramVStages) & 1), &b.fail, p.err)) break;
+        if (!wait_phase(&b.h_full[hs], (uint32_t)((j / kGramHStages) & 1), &b.fail, p.err)) break;
+        tc::fence_after_sync();
+        const uint32_t va = vring + vs * kTileBytes, hi = hring + 2 * hs * kTileBytes, lo = hi + kTileBytes;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int fb = fb0 + 8 * h;
-      uint4 tr[8];
-      transpose8x8(raw[h], tr);
-#pragma unroll
-      for (int f = 0; f < 8; ++f)
-        *reinterpret_cast<uint4*>(smem + tc::sw128_offset(8 * fb + f, tb, kTile)) = tr[f];
-      uint4 hi[8], lo[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        float x[8];
-        bf16x8_to_f32(raw[h][t], x);
-        float y[8], yh[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) y[q] = x[q] * asq[t];
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          hw[q] = pack_bf16x2(y[2 * q], y[2 * q + 1]);
-          yh[2 * q] = __uint_as_float(hw[q] << 16);
-          yh[2 * q + 1] = __uint_as_float(hw[q] & 0xffff0000u);
-          lw[q] = pack_bf16x2(y[2 * q] - yh[2 * q], y[2 * q + 1] - yh[2 * q + 1]);
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+          const uint32_t off = (uint32_t)ks * 2048u;   // 16 tokens = two 8-token groups of 1024 bytes
+          const uint64_t ad = tc::sw128_desc_mn(va + off, kTileBytes / 2, 1024);
+          tc::mma_bf16(tmem, ad, tc::sw128_desc_mn(hi + off, kTileBytes / 2, 1024), idesc, (j > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_bf16(tmem, ad, tc::sw128_desc_mn(lo + off, kTileBytes / 2, 1024), idesc, 1u);
         }
-        hi[t] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        lo[t] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        tc::mma_commit(&b.v_empty[vs]);
+        tc::mma_commit(&b.h_empty[hs]);
       }
-      transpose8x8(hi, tr);
-#pragma unroll
-      for (int f = 0; f < 8; ++f)
-        *reinterpret_cast<uint4*>(smem + kTileBytes + tc::sw128_offset(8 * fb + f, tb, kTile)) = tr[f];
-      transpose8x8(lo, tr);
-#pragma unroll
-      for (int f = 0; f < 8; ++f)
-        *reinterpret_cast<uint4*>(smem + 2 * kTileBytes + tc::sw128_offset(8 * fb + f, tb, kTile)) = tr[f];
+      tc::mma_commit(&b.done);                          // after every MMA issued (also on a failure)
+      drain_phase(&b.done, 0, p.err);                   // none may run once TMEM is released
     }
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (s_fail) break;
-    if (tid == 0) {
-      tc::fence_after_sync();
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTile, kTile);
+    __syncwarp();
+  } else {                                              // converters: a^2 v -> bf16 hi + lo
+    const int ct = tid - 64;                            // 0 .. 255
+    const int p16 = ct & 7;                             // 16-byte chunk position inside a row
+    const float* attn = p.attn + (size_t)bh * p.rows;
+    // this thread's four tokens' weights a^2, loaded one tile ahead
+    float asq_next[4];
+    auto load_asq = [&](int i, float (&dst)[4]) {
+      const bool kept = i < Ck;
+      const int base = kept ? kTile * i : p.k + kTile * (i - Ck);
+      const int lim = kept ? p.k : p.k + p.m;
 #pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        const uint32_t off = (uint32_t)((st >> 2) * kTile * 128 + (st & 3) * 32);
-        const uint64_t ad = tc::sw128_desc(a_tile + off);
-        tc::mma_bf16(tmem, ad, tc::sw128_desc(bhi_tile + off), idesc, (t0 > r_begin || st > 0) ? 1u : 0u);
-        tc::mma_bf16(tmem, ad, tc::sw128_desc(blo_tile + off), idesc, 1u);
+      for (int rr = 0; rr < 4; ++rr) {
+        const int gi = base + (ct >> 3) + 32 * rr;
+        const float av = (i < t1 && gi < lim) ? attn[gi] : 0.f;
+        dst[rr] = av * av;
       }
-      tc::mma_commit(&bar);
+    };
+    load_asq(t0, asq_next);
+    for (int i = t0; i < t1; ++i) {
+      const int j = i - t0, vs = j % kGramVStages, hs = j % kGramHStages;
+      float asq_cur[4];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) asq_cur[rr] = asq_next[rr];
+      load_asq(i + 1, asq_next);
+      bool ok = wait_phase(&b.v_full[vs], (uint32_t)((j / kGramVStages) & 1), &b.fail, p.err);
+      ok = ok && wait_phase(&b.h_empty[hs], (uint32_t)(((j / kGramHStages) & 1) ^ 1), &b.fail, p.err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const unsigned char* vt = smem + vs * kTileBytes;
+      unsigned char* ht = smem + (kGramVStages + 2 * hs) * kTileBytes;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int row = (ct >> 3) + 32 * rr;            // token of this thread's chunks
+        const uint64_t asq2 = pack_f32x2(asq_cur[rr], asq_cur[rr]);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int off = hf * (kTileBytes / 2) + row * 128 + p16 * 16;
+          const uint4 raw = *reinterpret_cast<const uint4*>(vt + off);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint64_t y = mul_f32x2(pack_f32x2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u)), asq2);
+            const float y0 = __uint_as_float((uint32_t)y), y1 = __uint_as_float((uint32_t)(y >> 32));
+            hw[q] = pack_bf16x2(y0, y1);
+            const uint64_t r = sub_f32x2(y, pack_f32x2(__uint_as_float(hw[q] << 16), __uint_as_float(hw[q] & 0xffff0000u)));
+            lw[q] = pack_bf16x2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+          }
+          *reinterpret_cast<uint4*>(ht + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(ht + kTileBytes + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&b.h_full[hs]);
     }
-    pending = 1;
-    if (t0 + kTile < r_end) load_tile(t0 + kTile);          // overlaps with the MMAs
-  }
-  // the last commit (also on a failure path, so no MMA is in flight at dealloc)
-  if (pending && !wait_mma(&bar, parity, p.err)) s_fail = 1;
-  __syncthreads();
-  tc::fence_after_sync();
-  if (!s_fail) {
-    float* out = p.gram_part + ((size_t)bh * p.splits + split) * kHeadDim * kHeadDim + (size_t)tid * kHeadDim;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    // accumulator -> reduction buffer (row f = feature, padded rows); the two
+    // warps of a TMEM lane quarter take 64 columns each
+    const bool have = t1 > t0;
+    bool ok = !have || wait_phase(&b.done, 0, &b.fail, p.err);
+    ok = __all_sync(0xffffffffu, ok);
+    tc::fence_after_sync();
+    const int f = 32 * (warp & 3) + lane;               // TMEM lane quarter of this warp
+    const int cbase = ((warp - 2) >> 2) * 64;
+    float* red = reinterpret_cast<float*>(smem) + (size_t)f * kGramRedPitch;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kTile; c0 += 32) {
+    for (int c0 = cbase; c0 < cbase + 64; c0 += 32) {
       float v[32];
-      tc::tmem_ld32(trow + c0, v);
+      if (have && ok) {
+        tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0, v);
+      } else {
 #pragma unroll
-      for (int c = 0; c < 32; c += 4)
-        *reinterpret_cast<float4*>(out + c0 + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+        for (int c = 0; c < 32; ++c) v[c] = 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(red + c0 + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
     }
   }
   tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, kTile);
+  tc::cluster_sync();                                   // every partial is in its CTA's shared memory
+  tc::fence_after_sync();
+  {
+    const int rows_per = (kHeadDim + S - 1) / S;
+    const int f0 = rank * rows_per, f1 = min(kHeadDim, f0 + rows_per);
+    float* out = p.gram + (size_t)bh * kHeadDim * kHeadDim;
+    const uint32_t red0 = tc::smem_u32(smem);
+    for (int item = tid; item < (f1 - f0) * (kHeadDim / 4); item += kGramThreads) {
+      const int f = f0 + item / (kHeadDim / 4), c = 4 * (item % (kHeadDim / 4));
+      const uint32_t off = (uint32_t)((f * kGramRedPitch + c) * 4);
+      float4 acc = tc::ld_cluster_f4(tc::map_to_rank(red0 + off, 0));
+      for (int sr = 1; sr < S; ++sr) {
+        const float4 v = tc::ld_cluster_f4(tc::map_to_rank(red0 + off, (uint32_t)sr));
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      *reinterpret_cast<float4*>(out + (size_t)f * kHeadDim + c) = acc;
+    }
+  }
+  tc::cluster_sync();                                   // no CTA leaves while others read its memory
+  if (warp == 2) tc::tmem_dealloc(tmem, kTile);
 }
 
 // ---------------------------------------------------------------------------
-// Top-r eigenvectors of G (symmetric, 128 x 128), one CTA of 512 threads per
-// (b, h). G is normalised by its trace and held in registers: kGroup threads
-// share a row, thread t owning row t/kGroup and the columns c = t%kGroup
-// (mod kGroup).
+// Top-r eigenvectors of G (symmetric, 128 x 128), one CTA of 128 threads per
+// (b, h). G is normalised by its trace and held in registers: warp w owns
+// rows 32 w .. +31 (whole rows, so A v needs no reduction across warps);
+// lane (lr, lc) = (lane / 8, lane % 8) owns rows R0 = 32 w + 8 lr .. +7 and
+// the columns 64 h + 8 lc .. +7 for h = 0, 1 (a[h][i][c]).
+//
+// Phases:
+//   1. Householder tridiagonalisation, one CTA barrier per step (below).
+//   2. Multisection (Sturm counts) for the top r eigenvalues of T.
+//   3. Inverse iteration on T (one lane per eigenvalue).
+//   4. Cholesky QR, two passes, to re-orthonormalise the r vectors.
+//   5. Back-transformation through the Householder reflections in blocks of
+//      eight (one reduction per block).
 // ---------------------------------------------------------------------------
-constexpr int kGroup = kEigThreads / kHeadDim; // threads per row
-constexpr int kEigPer = kHeadDim / kGroup;     // columns per thread
+constexpr int kEigSteps = kHeadDim - 2;            // Householder steps
+constexpr int kZPad = kHeadDim + 4;                // padded vector rows
+constexpr int kBtBlock = 8;                        // reflections per back-transform block
+constexpr int kBtBlocks = (kEigSteps + kBtBlock - 1) / kBtBlock;
+constexpr int kEigWarps = kEigThreads / 32;
+static_assert(kEigWarps == 4, "the eigensolver layout assumes four warps of 32 rows");
 
 struct EigSmem {
-  double trace;
-  double diag64[kHeadDim];
-  float hv[kHeadDim - 2][kHeadDim];   // Householder vector of step j (zeros up to index j)
-  float x[2][kHeadDim], pv[2][kHeadDim];
+  float hv[kEigSteps][kZPad];                      // Householder vector v_j (zeros up to index j)
+  float lu[5][kHeadDim][kCurdkvMaxRank];           // inverse-iteration LU factors, [factor][row][vector]
+  float z[kCurdkvMaxRank][kZPad];                  // eigenvectors (tridiagonal basis)
+  float zt[kHeadDim][kCurdkvMaxRank];              // the same during inverse iteration, [row][vector]
+  float vs[2][kHeadDim];                           // v of the step (by step parity)
+  float cb[2][kHeadDim];                           // the next column before the step's update
+  float pp[2][kHeadDim];                           // A v of the step
+  float kp[2][kEigWarps];                          // per-warp partials of v . A v
+  float wv[kEigWarps][3][kHeadDim];                // warp-private: v_{j-1}, w_{j-1}, x_j of every row
+  float vtv[kBtBlocks][kBtBlock][kBtBlock];        // v_k . v_m within a back-transform block
+  float beta[kHeadDim], d[kHeadDim], e[kHeadDim];
+  float2 de2[kHeadDim];                            // {d[i], e[i-1]^2} for the Sturm counts
   float gram[kCurdkvMaxRank][kCurdkvMaxRank + 1];
-  float d[kHeadDim], e[kHeadDim], e2[kHeadDim], beta[kHeadDim];
   float lam[kCurdkvMaxRank];
-  float z[kCurdkvMaxRank][kHeadDim];  // eigenvectors (tridiagonal basis, then original)
-  float lu[kCurdkvMaxRank][5][kHeadDim];  // per-vector LU factors: diag^-1, sup1, sup2, mult, pivot flag
+  double diag[kHeadDim];
+  double trace;
   float tnorm;
 };
-
-// Number of eigenvalues of the (normalised) tridiagonal T that are <= x.
-__device__ __forceinline__ int sturm_count(const EigSmem& s, float x, float pivmin) {
-  int cnt = 0;
-  float q = s.d[0] - x;
-  if (fabsf(q) < pivmin) q = -pivmin;
-  if (q <= 0.f) ++cnt;
-#pragma unroll 4
-  for (int i = 1; i < kHeadDim; ++i) {
-    q = s.d[i] - __fdividef(s.e2[i - 1], q) - x;
-    if (fabsf(q) < pivmin) q = -pivmin;
-    if (q <= 0.f) ++cnt;
-  }
-  return cnt;
-}
 
 __device__ __forceinline__ float hash_unit(int i, int j) {
   uint32_t h = (uint32_t)i * 2654435761u ^ (uint32_t)(j + 1) * 2246822519u;
@@ -794,39 +863,96 @@ __device__ __forceinline__ float hash_unit(int i, int j) {
   return (float)(h & 0xFFFFu) * (1.f / 65536.f) - 0.5f;
 }
 
+// Number of eigenvalues of the tridiagonal T that are <= x, for two shifts at
+// once: the sign changes of the leading principal minors of T - x I,
+//   p_0 = 1, p_1 = d_0 - x, p_{i+1} = (d_i - x) p_i - e_{i-1}^2 p_{i-1}.
+// This is the pivot recurrence q_i = p_i / p_{i-1} without its division
+// (the same rounding behaviour up to scaling); a minor smaller than 2^-24 of
+// its predecessor counts as a negative pivot, and every second step both
+// minors are rescaled by an exact power of two when they leave [2^-48, 2^48].
+__device__ __forceinline__ void sturm_count2(const float2* de2, const float (&x)[2], int (&cnt)[2]) {
+  constexpr float kTiny = 5.9604645e-08f;          // 2^-24
+  float u[2], v[2];
+  const float d0 = de2[0].x;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    u[k] = 1.f;
+    v[k] = d0 - x[k];
+    if (fabsf(v[k]) < kTiny) v[k] = -kTiny;
+    cnt[k] = v[k] < 0.f ? 1 : 0;
+  }
+  float2 tn = de2[1];
+#pragma unroll 2
+  for (int i = 1; i < kHeadDim; ++i) {
+    const float2 t = tn;
+    if (i + 1 < kHeadDim) tn = de2[i + 1];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float g = kTiny * v[k];
+      float w = fmaf(t.x - x[k], v[k], -t.y * u[k]);
+      if (fabsf(w) < fabsf(g)) w = -g;
+      cnt[k] += (int)((__float_as_uint(w) ^ __float_as_uint(v[k])) >> 31);
+      u[k] = v[k];
+      v[k] = w;
+    }
+    if (i & 1) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int ex = (int)((__float_as_uint(fmaxf(fabsf(u[k]), fabsf(v[k]))) >> 23) & 0xff) - 127;
+        const float sc = (ex > 48 || ex < -48) ? __uint_as_float((uint32_t)(127 - ex) << 23) : 1.f;
+        u[k] *= sc;
+        v[k] *= sc;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float eig_xval(float cbq, float vq, float wq, float omega, float nu) {
+  return fmaf(-vq, omega, fmaf(-wq, nu, cbq));
+}
+
+template <bool kBoth>
+struct EigHalves {
+  static constexpr int kFirst = kBoth ? 0 : 1;     // first live column half
+  static constexpr int kOwnHalf = kBoth ? 0 : 1;   // half holding column j + 1
+};
+
 __global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(16) unsigned char eig_raw[];
   EigSmem& s = *reinterpret_cast<EigSmem*>(eig_raw);
   const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int n = kHeadDim;
-  constexpr int kWarps = kEigThreads / 32;
   const int r = p.rank;
   float* evec_out = p.evec + (size_t)bh * kCurdkvMaxRank * n;
-  const int row = tid / kGroup, q4 = tid % kGroup;   // q4: this thread's column class
+  const int lr = lane >> 3, lc = lane & 7;
+  const int R0 = 32 * warp + 8 * lr;
 
-  // G = sum of the partials in a fixed order: fp32, except the diagonal terms
-  // that form E = trace G (fp64; GB300's fp64 rate is low, so only those)
-  const int splits_used = (p.n + kGramRows - 1) / kGramRows;
-  const float* part = p.gram_part + (size_t)bh * p.splits * n * n + row * n + q4;
-  float a[kEigPer];
+  // --- G (summed by the Gram kernel's cluster); E = trace G in fp64 --------
+  float a[2][8][8];
+  {
+    const float* src = p.gram + (size_t)bh * n * n + (size_t)R0 * n + 8 * lc;
 #pragma unroll
-  for (int i = 0; i < kEigPer; ++i) a[i] = 0.f;
-  for (int sp = 0; sp < splits_used; ++sp) {        // branch-free so the loads overlap
-    const float* src = part + (size_t)sp * n * n;
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int i = 0; i < kEigPer; ++i) a[i] += src[kGroup * i];
+      for (int i = 0; i < 8; ++i) {
+        const float4 u0 = __ldg(reinterpret_cast<const float4*>(src + i * n + 64 * h));
+        const float4 u1 = __ldg(reinterpret_cast<const float4*>(src + i * n + 64 * h + 4));
+        a[h][i][0] = u0.x; a[h][i][1] = u0.y; a[h][i][2] = u0.z; a[h][i][3] = u0.w;
+        a[h][i][4] = u1.x; a[h][i][5] = u1.y; a[h][i][6] = u1.z; a[h][i][7] = u1.w;
+      }
   }
-  if (row % kGroup == q4) {                          // this thread holds G[row][row]
-    const float* src = p.gram_part + (size_t)bh * p.splits * n * n + row * n + row;
-    double diag = 0.0;
-    for (int sp = 0; sp < splits_used; ++sp) diag += src[(size_t)sp * n * n];
-    s.diag64[row] = diag;
-  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (R0 == 64 * h + 8 * lc) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s.diag[R0 + i] = (double)a[h][i][i];
+    }
   __syncthreads();
-  if (tid == 0) {
-    double tr = 0.0;
-    for (int i = 0; i < n; ++i) tr += s.diag64[i];
-    s.trace = tr;
+  if (warp == 0) {
+    double t = ((s.diag[4 * lane] + s.diag[4 * lane + 1]) + s.diag[4 * lane + 2]) + s.diag[4 * lane + 3];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) s.trace = t;
   }
   __syncthreads();
   if (!(s.trace > 0.0)) {
@@ -836,374 +962,663 @@ __global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid
   }
   if (tid == 0) p.inv_e[bh] = (float)(1.0 / s.trace);
   {
-    const float sc = (float)(1.0 / s.trace);     // normalise: eigenvectors unchanged
+    const float sc = (float)(1.0 / s.trace);         // normalise: eigenvectors unchanged
 #pragma unroll
-    for (int i = 0; i < kEigPer; ++i) a[i] *= sc;
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) a[h][i][c] *= sc;
   }
 
-  // --- Householder tridiagonalisation (registers) ----------------------------
-  // a[i] holds column kGroup*(i + base) + q4; every kGroup steps the row
-  // shifts left by one (the finished columns drop out), so the column being
-  // reduced is always a[0], every register index is a compile-time constant
-  // and the loops stop at the last live column (a CTA-uniform bound).
-  // Step j works with x = column j below the diagonal, zero-filled up to
-  // index j in shared memory; the Householder vector v equals x except
-  // v[j+1] = x[j+1] + delta, which enters as one correction term. Each step
-  // has two barriers: every warp recomputes the step's scalars from the
-  // shared vectors (identical bits in every warp), and the vectors are
-  // double-buffered by step parity. Warps whose rows are all finished skip.
-  constexpr int kRowsPerWarp = 32 / kGroup;
-  int base = 0;
-  for (int j = 0; j < n - 2; ++j) {
-    float* xj = s.x[j & 1];
-    float* pj = s.pv[j & 1];
-    if (q4 == j % kGroup) {
-      xj[row] = row > j ? a[0] : 0.f;             // column j below the diagonal, zeros above
-      if (row == j) s.d[j] = a[0];                // diagonal element j
+  // --- 1. Householder tridiagonalisation -------------------------------------
+  // Step j: x = column j below the diagonal (zeros at rows <= j), sigma = |x|,
+  // v = x + delta e_{j+1}, beta = 2 / |v|^2, p = beta A v, K = beta/2 v.p,
+  // w = p - K v, A -= v w^T + w v^T (rows and columns > j only).
+  //
+  // One CTA barrier per step. Before the barrier of step j-1 the owners of
+  // column j publish it as it stands before step j-1's update (cb), and A v,
+  // the per-warp partials of v.A v and v itself are published. After it each
+  // warp forms, four rows per lane, w_{j-1} = beta A v - K v and
+  //   x_j = cb - v_{j-1} w_{j-1}[j] - w_{j-1} v_{j-1}[j]
+  // with |x_j|^2 (the same bits in every warp), keeps them in a warp-private
+  // buffer, and every thread applies step j-1's update fused with A x_j; the
+  // owners of column j+1 then add delta A[:, j+1] (v = x + delta e_{j+1}).
+  // The fused pass has no branch, so its multiply-adds overlap the scalar
+  // chain of the step; a warp whose rows are all finished computes values
+  // that nobody reads. After step 62 the first column half is finished and a
+  // second copy of the loop skips it.
+  if (lc == 0) {
+    *reinterpret_cast<float4*>(&s.cb[1][R0]) = make_float4(a[0][0][0], a[0][1][0], a[0][2][0], a[0][3][0]);
+    *reinterpret_cast<float4*>(&s.cb[1][R0 + 4]) = make_float4(a[0][4][0], a[0][5][0], a[0][6][0], a[0][7][0]);
+  }
+  s.vs[1][tid] = 0.f;
+  s.pp[1][tid] = 0.f;
+  if (tid < kEigWarps) s.kp[1][tid] = 0.f;
+  __syncthreads();
+
+  float beta_prev = 0.f;
+  float* wv = &s.wv[warp][0][0];
+  auto step = [&](auto both_tag, int j) {
+    constexpr bool kBoth = decltype(both_tag)::value;
+    constexpr int kFirst = EigHalves<kBoth>::kFirst, kOwnHalf = EigHalves<kBoth>::kOwnHalf;
+    const int b = j & 1, bp = b ^ 1;
+    float Kp;
+    {
+      const float4 k4 = *reinterpret_cast<const float4*>(&s.kp[bp][0]);
+      Kp = 0.5f * beta_prev * beta_prev * ((k4.x + k4.y) + (k4.z + k4.w));
     }
-    __syncthreads();
+    const float nu = s.vs[bp][j];
+    const float omega = fmaf(-Kp, nu, beta_prev * s.pp[bp][j]);
+    // v_{j-1}, w_{j-1}, x_j of rows 4 lane .. +3 (warp-private), |x_j|^2
     float ss = 0.f;
+    {
+      const int q0 = 4 * lane;
+      const float4 c4 = *reinterpret_cast<const float4*>(&s.cb[bp][q0]);
+      const float4 v4 = *reinterpret_cast<const float4*>(&s.vs[bp][q0]);
+      const float4 p4 = *reinterpret_cast<const float4*>(&s.pp[bp][q0]);
+      const float cq[4] = {c4.x, c4.y, c4.z, c4.w}, vq[4] = {v4.x, v4.y, v4.z, v4.w};
+      const float pq[4] = {p4.x, p4.y, p4.z, p4.w};
+      float wq[4], xq[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ss = fmaf(xj[32 * k + lane], xj[32 * k + lane], ss);
+      for (int k = 0; k < 4; ++k) {
+        const int q = q0 + k;
+        wq[k] = fmaf(-Kp, vq[k], q > j - 1 ? beta_prev * pq[k] : 0.f);
+        const float val = eig_xval(cq[k], vq[k], wq[k], omega, nu);
+        if (warp == 0 && q == j) s.d[j] = val;
+        xq[k] = q > j ? val : 0.f;
+        ss = fmaf(xq[k], xq[k], ss);
+      }
+      *reinterpret_cast<float4*>(wv + q0) = v4;
+      *reinterpret_cast<float4*>(wv + n + q0) = make_float4(wq[0], wq[1], wq[2], wq[3]);
+      *reinterpret_cast<float4*>(wv + 2 * n + q0) = make_float4(xq[0], xq[1], xq[2], xq[3]);
+    }
+    __syncwarp();
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float x0 = xj[j + 1];
+    const float x0 = wv[2 * n + j + 1];
     const float tail = ss - x0 * x0;
     float beta = 0.f, alpha = x0, delta = 0.f;
     if (tail > 0.f) {
-      const float sigma = sqrtf(ss);
+      const float sigma = ss * rsqrtf(ss);
       alpha = x0 >= 0.f ? -sigma : sigma;
-      delta = -alpha;                             // v[j+1] = x0 - alpha
-      beta = 1.f / (sigma * (sigma + fabsf(x0)));
+      delta = -alpha;                                   // v[j+1] = x0 - alpha
+      beta = __fdividef(1.f, sigma * (sigma + fabsf(x0)));
     }
-    if (warp == 0) {
+    // this thread's rows: v_{j-1}, w_{j-1}, x_j
+    float pvr[8], pwr[8], xr[8];
+    {
+      const float4 v0 = *reinterpret_cast<const float4*>(wv + R0), v1 = *reinterpret_cast<const float4*>(wv + R0 + 4);
+      const float4 w0 = *reinterpret_cast<const float4*>(wv + n + R0);
+      const float4 w1 = *reinterpret_cast<const float4*>(wv + n + R0 + 4);
+      const float4 x0v = *reinterpret_cast<const float4*>(wv + 2 * n + R0);
+      const float4 x1v = *reinterpret_cast<const float4*>(wv + 2 * n + R0 + 4);
+      pvr[0] = v0.x; pvr[1] = v0.y; pvr[2] = v0.z; pvr[3] = v0.w; pvr[4] = v1.x; pvr[5] = v1.y; pvr[6] = v1.z; pvr[7] = v1.w;
+      pwr[0] = w0.x; pwr[1] = w0.y; pwr[2] = w0.z; pwr[3] = w0.w; pwr[4] = w1.x; pwr[5] = w1.y; pwr[6] = w1.z; pwr[7] = w1.w;
+      xr[0] = x0v.x; xr[1] = x0v.y; xr[2] = x0v.z; xr[3] = x0v.w; xr[4] = x1v.x; xr[5] = x1v.y; xr[6] = x1v.z; xr[7] = x1v.w;
+    }
+    // step j-1's update fused with A x_j (column halves from kFirst)
+    float acc[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int c = 32 * k + lane;
-        const float xv = xj[c];
-        s.hv[j][c] = beta == 0.f ? 0.f : (c == j + 1 ? xv + delta : xv);
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int h = kFirst; h < 2; ++h) {
+      const int cb0 = 64 * h + 8 * lc;
+      float pvc[8], pwc[8], xc[8];
+      {
+        const float4 v0 = *reinterpret_cast<const float4*>(wv + cb0);
+        const float4 v1 = *reinterpret_cast<const float4*>(wv + cb0 + 4);
+        const float4 w0 = *reinterpret_cast<const float4*>(wv + n + cb0);
+        const float4 w1 = *reinterpret_cast<const float4*>(wv + n + cb0 + 4);
+        const float4 x0v = *reinterpret_cast<const float4*>(wv + 2 * n + cb0);
+        const float4 x1v = *reinterpret_cast<const float4*>(wv + 2 * n + cb0 + 4);
+        pvc[0] = v0.x; pvc[1] = v0.y; pvc[2] = v0.z; pvc[3] = v0.w; pvc[4] = v1.x; pvc[5] = v1.y; pvc[6] = v1.z; pvc[7] = v1.w;
+        pwc[0] = w0.x; pwc[1] = w0.y; pwc[2] = w0.z; pwc[3] = w0.w; pwc[4] = w1.x; pwc[5] = w1.y; pwc[6] = w1.z; pwc[7] = w1.w;
+        xc[0] = x0v.x; xc[1] = x0v.y; xc[2] = x0v.z; xc[3] = x0v.w; xc[4] = x1v.x; xc[5] = x1v.y; xc[6] = x1v.z; xc[7] = x1v.w;
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float val = fmaf(-pvr[i], pwc[c], fmaf(-pwr[i], pvc[c], a[h][i][c]));
+          a[h][i][c] = val;
+          acc[i] = fmaf(val, xc[c], acc[i]);
+        }
+    }
+    // column j+1 (updated through step j-1): delta A[:, j+1] completes A v_j;
+    // its owners publish it for the next step
+    const int j1 = j + 1;
+    const bool own1 = 64 * kOwnHalf + 8 * lc == (j1 & ~7);
+    float col[8];
+    switch (j1 & 7) {
+#define EIG_COL_CASE(c)                                                 \
+  case c:                                                               \
+    for (int i = 0; i < 8; ++i) col[i] = a[kOwnHalf][i][c];             \
+    break;
+      EIG_COL_CASE(0) EIG_COL_CASE(1) EIG_COL_CASE(2) EIG_COL_CASE(3)
+      EIG_COL_CASE(4) EIG_COL_CASE(5) EIG_COL_CASE(6) EIG_COL_CASE(7)
+#undef EIG_COL_CASE
+    }
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      acc[i] = own1 ? fmaf(delta, col[i], acc[i]) : acc[i];
+      const float vr = xr[i] + (R0 + i == j1 ? delta : 0.f);
+      t = fmaf(vr, acc[i], t);
+    }
+    // reduce-scatter over the 8 column lanes: lane lc ends with row R0 + lc
+    const bool h4 = lc & 4, h2 = lc & 2, h1 = lc & 1;
+    float s4[4], s2[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float keep = h4 ? acc[4 + i] : acc[i];
+      const float send = h4 ? acc[i] : acc[4 + i];
+      s4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float keep = h2 ? s4[2 + i] : s4[i];
+      const float send = h2 ? s4[i] : s4[2 + i];
+      s2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    const float s1 = (h1 ? s2[1] : s2[0]) + __shfl_xor_sync(0xffffffffu, h1 ? s2[0] : s2[1], 1);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    s.pp[b][R0 + lc] = s1;
+    if (lane == 0) s.kp[b][warp] = 32 * warp + 31 > j ? t : 0.f;   // finished rows: v is zero there
+    if (own1) {
+      *reinterpret_cast<float4*>(&s.cb[b][R0]) = make_float4(col[0], col[1], col[2], col[3]);
+      *reinterpret_cast<float4*>(&s.cb[b][R0 + 4]) = make_float4(col[4], col[5], col[6], col[7]);
+    }
+    if (warp == 0) {                                    // v_j for the next step and the back-transform
+      const int q0 = 4 * lane;
+      const float4 x4 = *reinterpret_cast<const float4*>(wv + 2 * n + q0);
+      float4 v4;
+      v4.x = x4.x + (q0 == j1 ? delta : 0.f);
+      v4.y = x4.y + (q0 + 1 == j1 ? delta : 0.f);
+      v4.z = x4.z + (q0 + 2 == j1 ? delta : 0.f);
+      v4.w = x4.w + (q0 + 3 == j1 ? delta : 0.f);
+      *reinterpret_cast<float4*>(&s.vs[b][q0]) = v4;
+      *reinterpret_cast<float4*>(&s.hv[j][q0]) = v4;
       if (lane == 0) {
         s.beta[j] = beta;
         s.e[j] = alpha;
       }
     }
-    const bool live_rows = warp * kRowsPerWarp + kRowsPerWarp - 1 > j;   // some row of this warp is > j
-    // index of column j+1 in this thread's registers, if this thread owns it
-    const bool owns_next = q4 == (j + 1) % kGroup;
-    const int next_idx = (j + 1) / kGroup - base;      // 0 or 1
-    if (beta != 0.f) {
-      // p = beta * A v = beta * (A x + A[:, j+1] * delta)
-      float acc = 0.f;
-      if (live_rows) {
-        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < kEigPer; ++i) {
-          if (i + base >= kEigPer) break;
-          const float xc = xj[kGroup * (i + base) + q4];
-          if (i & 1) acc1 = fmaf(a[i], xc, acc1); else acc0 = fmaf(a[i], xc, acc0);
-        }
-        acc = acc0 + acc1;
-        if (owns_next) acc = fmaf(next_idx == 0 ? a[0] : a[1], delta, acc);
-#pragma unroll
-        for (int o = 1; o < kGroup; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      }
-      if (q4 == 0) pj[row] = row > j ? beta * acc : 0.f;
-      __syncthreads();
-      // K = beta/2 * v.p, recomputed by every warp (p is zero up to index j)
-      float dot = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) dot = fmaf(xj[32 * k + lane], pj[32 * k + lane], dot);
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      dot = fmaf(delta, pj[j + 1], dot);
-      const float K = 0.5f * beta * dot;
-      if (live_rows) {
-        // A -= v w^T + w v^T, w = p - K v; computed with x for v, then the
-        // column j+1 term corrected by delta * (w_r - K v_r)
-        const float vr = row > j ? xj[row] + (row == j + 1 ? delta : 0.f) : 0.f;
-        const float wr = pj[row] - K * vr;
-#pragma unroll
-        for (int i = 0; i < kEigPer; ++i) {
-          if (i + base >= kEigPer) break;
-          const int c = kGroup * (i + base) + q4;
-          const float xc = xj[c];
-          a[i] -= vr * fmaf(-K, xc, pj[c]) + wr * xc;
-        }
-        if (owns_next) {
-          const float corr = delta * (wr - K * vr);
-          if (next_idx == 0) a[0] -= corr; else a[1] -= corr;
-        }
-      }
+    beta_prev = beta;
+    __syncthreads();
+  };
+#pragma unroll 1
+  for (int j = 0; j < 63; ++j) step(std::true_type{}, j);
+#pragma unroll 1
+  for (int j = 63; j < kEigSteps; ++j) step(std::false_type{}, j);
+
+  // the trailing 2 x 2 block after the last step's update
+  {
+    constexpr int bp = (kEigSteps & 1) ^ 1;            // the last step's buffers
+    float Kp;
+    {
+      const float4 k4 = *reinterpret_cast<const float4*>(&s.kp[bp][0]);
+      Kp = 0.5f * beta_prev * beta_prev * ((k4.x + k4.y) + (k4.z + k4.w));
     }
-    if (j % kGroup == kGroup - 1) {
-#pragma unroll
-      for (int i = 0; i < kEigPer - 1; ++i) a[i] = a[i + 1];
-      a[kEigPer - 1] = 0.f;
-      ++base;
+    auto w_at = [&](int q) { return fmaf(-Kp, s.vs[bp][q], beta_prev * s.pp[bp][q]); };
+    if (tid == 0) {
+      const float nu = s.vs[bp][n - 2], omega = w_at(n - 2);
+      s.d[n - 2] = eig_xval(s.cb[bp][n - 2], nu, omega, omega, nu);
+      s.e[n - 2] = eig_xval(s.cb[bp][n - 1], s.vs[bp][n - 1], w_at(n - 1), omega, nu);
+      s.e[n - 1] = 0.f;
+    }
+    if (R0 == n - 8 && lc == 7) {
+      const float v7 = s.vs[bp][n - 1], w7 = w_at(n - 1);
+      s.d[n - 1] = fmaf(-v7, w7, fmaf(-w7, v7, a[1][7][7]));
     }
   }
-  // last 2 x 2 block: after (n-2)/kGroup shifts a[0] holds column n-2-(n-2)%kGroup + q4
-  static_assert((kHeadDim - 2) % kGroup + 1 < kGroup, "columns n-2 and n-1 share a[0]");
-  if (row == n - 2 && q4 == (n - 2) % kGroup) s.d[n - 2] = a[0];
-  if (row == n - 1 && q4 == (n - 2) % kGroup) s.e[n - 2] = a[0];
-  if (row == n - 1 && q4 == (n - 1) % kGroup) s.d[n - 1] = a[0];
   __syncthreads();
-  if (tid == 0) {
-    s.e[n - 1] = 0.f;
+  if (warp == 0) {
     float tn = 0.f;
-    for (int i = 0; i < n; ++i) {
-      const float rad = fabsf(s.d[i]) + fabsf(s.e[i]) + (i > 0 ? fabsf(s.e[i - 1]) : 0.f);
-      tn = fmaxf(tn, rad);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = 4 * lane + k;
+      const float em = i > 0 ? s.e[i - 1] : 0.f;
+      tn = fmaxf(tn, fabsf(s.d[i]) + fabsf(s.e[i]) + fabsf(em));
+      s.de2[i] = make_float2(s.d[i], em * em);
     }
-    s.tnorm = fmaxf(tn, FLT_MIN);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) tn = fmaxf(tn, __shfl_xor_sync(0xffffffffu, tn, o));
+    if (lane == 0) s.tnorm = fmaxf(tn, FLT_MIN);
   }
   __syncthreads();
-  if (tid < n) s.e2[tid] = s.e[tid] * s.e[tid];
-  __syncthreads();
 
-  // --- top r eigenvalues by multisection (one warp per eigenvalue) ----------
+  // --- 2. top r eigenvalues by multisection (8 threads x 2 shifts each) -------
   const float tnorm = s.tnorm;
-  const float pivmin = FLT_MIN * 1e4f;
-  for (int jj = warp; jj < r; jj += kWarps) {
-    const int target = n - 1 - jj;                   // ascending index
-    float lo = -tnorm * 1.01f - pivmin, hi = tnorm * 1.01f + pivmin;
-    for (int round = 0; round < 8; ++round) {
-      const float step = (hi - lo) / 33.f;
-      const float xv = lo + step * (float)(lane + 1);
-      const int cnt = sturm_count(s, xv, pivmin);
-      const unsigned above = __ballot_sync(0xffffffffu, cnt >= target + 1);
-      const int first = above ? __ffs(above) - 1 : 32;
-      const float nlo = first == 0 ? lo : lo + step * (float)first;
-      const float nhi = first == 32 ? hi : lo + step * (float)(first + 1);
-      lo = nlo;
-      hi = nhi;
-      if (hi - lo <= 2.f * FLT_EPSILON * fmaxf(fabsf(lo), fabsf(hi)) + pivmin) break;
+  {
+    const int grp = tid >> 3, sub = tid & 7;          // eigenvalue grp, 16 shifts per round
+    const unsigned gmask = 0xffu << (lane & 24);
+    for (int jj = grp; jj < r; jj += kEigThreads / 8) {
+      const int target = n - 1 - jj;                  // ascending index
+      float lo = -tnorm * 1.01f, hi = tnorm * 1.01f;
+      for (int round = 0; round < 6; ++round) {       // 17^6: width below 1e-7 tnorm
+        const float step = (hi - lo) / 17.f;
+        float xv[2];
+        int cnt[2];
+        xv[0] = lo + step * (float)(2 * sub + 1);
+        xv[1] = lo + step * (float)(2 * sub + 2);
+        sturm_count2(s.de2, xv, cnt);
+        int first = 16;                               // first shift with count > target
+        if (cnt[1] >= target + 1) first = 2 * sub + 1;
+        if (cnt[0] >= target + 1) first = 2 * sub;
+        first = (int)__reduce_min_sync(gmask, (unsigned)first);
+        const float nlo = first == 0 ? lo : lo + step * (float)first;
+        const float nhi = first == 16 ? hi : lo + step * (float)(first + 1);
+        lo = nlo;
+        hi = nhi;
+        if (hi - lo <= 2.f * FLT_EPSILON * fmaxf(fabsf(lo), fabsf(hi))) break;
+      }
+      if (sub == 0) s.lam[jj] = 0.5f * (lo + hi);
     }
-    if (lane == 0) s.lam[jj] = 0.5f * (lo + hi);
   }
   __syncthreads();
 
-  // --- inverse iteration (lane 0 of one warp per eigenvalue) -----------------
-  const float guard = FLT_EPSILON * tnorm;
-  for (int jj = warp; jj < r; jj += kWarps) {
-    float* rd = s.lu[jj][0];
-    float* u1 = s.lu[jj][1];
-    float* u2 = s.lu[jj][2];
-    float* ml = s.lu[jj][3];
-    float* pf = s.lu[jj][4];
-    float* zz = s.z[jj];
-    for (int i = lane; i < n; i += 32) zz[i] = hash_unit(i, jj) + 0.75f;
-    __syncwarp();
-    if (lane == 0) {
-      const float lam = s.lam[jj];
-      // LU with partial pivoting of T - lam I (rows: sub e[i-1], diag d[i]-lam, super e[i]);
-      // rd holds the reciprocals of U's (guarded) diagonal
-      float cd = s.d[0] - lam, cs = s.e[0];
-      for (int i = 0; i < n - 1; ++i) {
-        const float sub = s.e[i], nd = s.d[i + 1] - lam, ns = s.e[i + 1];
-        if (fabsf(cd) >= fabsf(sub)) {
-          if (fabsf(cd) < guard) cd = cd < 0.f ? -guard : guard;
-          const float inv = 1.f / cd;
-          const float l = sub * inv;
-          rd[i] = inv; u1[i] = cs; u2[i] = 0.f; ml[i] = l; pf[i] = 0.f;
-          cd = nd - l * cs;
-          cs = ns;
-        } else {
-          const float l = cd / sub;
-          const float dg = fabsf(sub) < guard ? (sub < 0.f ? -guard : guard) : sub;
-          rd[i] = 1.f / dg; u1[i] = nd; u2[i] = ns; ml[i] = l; pf[i] = 1.f;
-          cd = cs - l * nd;
-          cs = -l * ns;
-        }
-      }
-      if (fabsf(cd) < guard) cd = cd < 0.f ? -guard : guard;
-      rd[n - 1] = 1.f / cd; u1[n - 1] = 0.f; u2[n - 1] = 0.f;
-      for (int it = 0; it < 2; ++it) {
-        for (int i = 0; i < n - 1; ++i) {
-          if (pf[i] != 0.f) {
-            const float t = zz[i];
-            zz[i] = zz[i + 1];
-            zz[i + 1] = t - ml[i] * zz[i + 1];
-          } else {
-            zz[i + 1] -= ml[i] * zz[i];
-          }
-        }
-        zz[n - 1] = zz[n - 1] * rd[n - 1];
-        zz[n - 2] = (zz[n - 2] - u1[n - 2] * zz[n - 1]) * rd[n - 2];
-        float mx = fmaxf(fabsf(zz[n - 1]), fabsf(zz[n - 2]));
-        for (int i = n - 3; i >= 0; --i) {
-          zz[i] = (zz[i] - u1[i] * zz[i + 1] - u2[i] * zz[i + 2]) * rd[i];
-          mx = fmaxf(mx, fabsf(zz[i]));
-        }
-        const float inv = mx > 0.f ? 1.f / mx : 0.f;
-        for (int i = 0; i < n; ++i) zz[i] *= inv;
-      }
+  // --- 3. inverse iteration: lane jj of warp 0, vector in registers ----------
+  if (warp == 0 && lane < r) {
+    const int jj = lane;
+    const float lam = s.lam[jj];
+    const float guard = FLT_EPSILON * tnorm;
+    // LU with partial pivoting of T - lam I (rows: sub e[i-1], diag d[i]-lam, super e[i])
+    float cd = s.d[0] - lam, cs = s.e[0];
+#pragma unroll 2
+    for (int i = 0; i < n - 1; ++i) {
+      const float sub = s.e[i], nd = s.d[i + 1] - lam, ns = s.e[i + 1];
+      const bool piv = fabsf(cd) < fabsf(sub);
+      float ud = piv ? sub : cd;
+      if (fabsf(ud) < guard) ud = ud < 0.f ? -guard : guard;
+      const float rinv = __fdividef(1.f, ud);
+      const float l = (piv ? cd : sub) * rinv;
+      s.lu[0][i][jj] = rinv;
+      s.lu[1][i][jj] = piv ? nd : cs;
+      s.lu[2][i][jj] = piv ? ns : 0.f;
+      s.lu[3][i][jj] = l;
+      s.lu[4][i][jj] = piv ? 1.f : 0.f;
+      const float ncd = piv ? fmaf(-l, nd, cs) : fmaf(-l, cs, nd);
+      cs = piv ? -l * ns : ns;
+      cd = ncd;
     }
-    __syncwarp();
+    if (fabsf(cd) < guard) cd = cd < 0.f ? -guard : guard;
+    s.lu[0][n - 1][jj] = __fdividef(1.f, cd);
+    // the vector lives in shared memory ([row][vector]: conflict-free); each
+    // recurrence keeps its running values in registers, so the dependency
+    // chains never pass through memory
+    for (int i = 0; i < n; ++i) s.zt[i][jj] = hash_unit(i, jj) + 0.75f;
+#pragma unroll 1
+    for (int it = 0; it < 2; ++it) {
+      float cur = s.zt[0][jj];
+#pragma unroll 4
+      for (int i = 0; i < n - 1; ++i) {               // row interchanges and L
+        const bool pv = s.lu[4][i][jj] != 0.f;
+        const float ml = s.lu[3][i][jj];
+        const float nxt = s.zt[i + 1][jj];
+        s.zt[i][jj] = pv ? nxt : cur;
+        cur = pv ? fmaf(-ml, nxt, cur) : fmaf(-ml, cur, nxt);
+      }
+      float z2 = cur * s.lu[0][n - 1][jj];            // back substitution with U
+      float z1 = fmaf(-s.lu[1][n - 2][jj], z2, s.zt[n - 2][jj]) * s.lu[0][n - 2][jj];
+      s.zt[n - 1][jj] = z2;
+      s.zt[n - 2][jj] = z1;
+      float mx = fmaxf(fabsf(z1), fabsf(z2));
+#pragma unroll 4
+      for (int i = n - 3; i >= 0; --i) {
+        const float z0 = fmaf(-s.lu[2][i][jj], z2, fmaf(-s.lu[1][i][jj], z1, s.zt[i][jj])) * s.lu[0][i][jj];
+        s.zt[i][jj] = z0;
+        mx = fmaxf(mx, fabsf(z0));
+        z2 = z1;
+        z1 = z0;
+      }
+      const float inv = mx > 0.f ? 1.f / mx : 0.f;
+      for (int i = 0; i < n; ++i) s.zt[i][jj] *= inv;
+    }
+  }
+  __syncthreads();
+  for (int el = tid; el < r * n; el += kEigThreads) s.z[el / n][el % n] = s.zt[el % n][el / n];
+  // v_k . v_m inside each back-transform block (independent of the eigenvectors):
+  // eight threads per block, lane q of the eight holding elements 4q + 32i + 0..3
+  {
+    const int g = tid >> 3, q = tid & 7;
+    const unsigned gmask = 0xffu << (lane & 24);
+    for (int blk = g; blk < kBtBlocks; blk += kEigThreads / 8) {
+      const int j0 = blk * kBtBlock;
+      float hvq[kBtBlock][16];
+#pragma unroll
+      for (int k = 0; k < kBtBlock; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j0 + k < kEigSteps) u = *reinterpret_cast<const float4*>(&s.hv[j0 + k][4 * q + 32 * i]);
+          hvq[k][4 * i] = u.x; hvq[k][4 * i + 1] = u.y; hvq[k][4 * i + 2] = u.z; hvq[k][4 * i + 3] = u.w;
+        }
+#pragma unroll
+      for (int k = 0; k < kBtBlock; ++k)
+#pragma unroll
+        for (int m = k + 1; m < kBtBlock; ++m) {
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dot = fmaf(hvq[k][e], hvq[m][e], dot);
+#pragma unroll
+          for (int o = 4; o >= 1; o >>= 1) dot += __shfl_xor_sync(gmask, dot, o);
+          if (q == 0) s.vtv[blk][k][m] = dot;           // zero past the last reflection
+        }
+    }
   }
   __syncthreads();
 
-  // --- orthonormalise the r vectors: Cholesky-QR, two passes ---------------
-  // M = Z Z^T = L L^T, Z <- L^{-1} Z. A non-positive pivot (a dependent
+  // --- 4. orthonormalise the r vectors: Cholesky QR, two passes ---------------
+  // M = Z Z^T = L L^T, Z <- L^{-1} Z; a non-positive pivot (a dependent
   // vector) drops that vector.
   for (int pass = 0; pass < 2; ++pass) {
-    for (int pr = warp; pr < r * r; pr += kWarps) {
-      const int ia = pr / r, ib = pr % r;
-      if (ib > ia) continue;
-      float dot = 0.f;
+    {                                                   // M = Z Z^T: eight threads per row ia, all ib <= ia
+      const int g = tid >> 3, q = tid & 7;
+      const unsigned gmask = 0xffu << (lane & 24);
+      for (int ia = g; ia < r; ia += kEigThreads / 8) {
+        float za[16];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) dot = fmaf(s.z[ia][32 * k + lane], s.z[ib][32 * k + lane], dot);
+        for (int i = 0; i < 4; ++i) {
+          const float4 u = *reinterpret_cast<const float4*>(&s.z[ia][4 * q + 32 * i]);
+          za[4 * i] = u.x; za[4 * i + 1] = u.y; za[4 * i + 2] = u.z; za[4 * i + 3] = u.w;
+        }
+#pragma unroll 4
+        for (int ib = 0; ib <= ia; ++ib) {
+          float dot = 0.f;
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      if (lane == 0) s.gram[ia][ib] = dot;
+          for (int i = 0; i < 4; ++i) {
+            const float4 u = *reinterpret_cast<const float4*>(&s.z[ib][4 * q + 32 * i]);
+            dot = fmaf(za[4 * i], u.x, fmaf(za[4 * i + 1], u.y, fmaf(za[4 * i + 2], u.z, fmaf(za[4 * i + 3], u.w, dot))));
+          }
+#pragma unroll
+          for (int o = 4; o >= 1; o >>= 1) dot += __shfl_xor_sync(gmask, dot, o);
+          if (q == 0) {
+            s.gram[ia][ib] = dot;
+            s.gram[ib][ia] = dot;
+          }
+        }
+      }
     }
     __syncthreads();
-    if (warp == 0) {                                   // in-place lower Cholesky factor, lane = row
+    if (warp == 0) {                                    // right-looking Cholesky in place, lane = row
       for (int k = 0; k < r; ++k) {
-        // row k's entries left of the diagonal are final: finish column k
-        float dkk = 0.f;
-        if (lane == k) {
-          float acc = s.gram[k][k];
-          for (int m = 0; m < k; ++m) acc -= s.gram[k][m] * s.gram[k][m];
-          dkk = acc > 1e-20f ? sqrtf(acc) : 0.f;
-          s.gram[k][k] = dkk;
-        }
-        dkk = __shfl_sync(0xffffffffu, dkk, k);
+        const float dk = s.gram[k][k];
+        const float dinv = dk > 1e-20f ? rsqrtf(dk) : 0.f;
+        if (lane >= k && lane < r) s.gram[lane][k] *= dinv;   // L[k][k] = sqrt(dk)
+        if (lane == 0) s.lam[k] = dinv;                        // reciprocal pivots
+        __syncwarp();
         if (lane > k && lane < r) {
-          float acc = s.gram[lane][k];
-          for (int m = 0; m < k; ++m) acc -= s.gram[lane][m] * s.gram[k][m];
-          s.gram[lane][k] = dkk > 0.f ? acc / dkk : 0.f;
+          const float lik = s.gram[lane][k];
+#pragma unroll 4
+          for (int m = k + 1; m <= lane; ++m) s.gram[lane][m] = fmaf(-lik, s.gram[m][k], s.gram[lane][m]);
         }
         __syncwarp();
       }
     }
     __syncthreads();
-    if (tid < n) {                                     // forward substitution in place, one column per thread
+    if (tid < n) {                                      // forward substitution in place, one column per thread
+#pragma unroll 1
       for (int ia = 0; ia < r; ++ia) {
         float acc = s.z[ia][tid];
-        for (int ib = 0; ib < ia; ++ib) acc -= s.gram[ia][ib] * s.z[ib][tid];
-        s.z[ia][tid] = s.gram[ia][ia] > 0.f ? acc / s.gram[ia][ia] : 0.f;
+#pragma unroll 4
+        for (int ib = 0; ib < ia; ++ib) acc = fmaf(-s.gram[ia][ib], s.z[ib][tid], acc);
+        s.z[ia][tid] = acc * s.lam[ia];
       }
     }
     __syncthreads();
   }
 
-  // --- back-transform: y = H_0 H_1 ... H_{n-3} z  (one warp per vector) -----
-  for (int jj = warp; jj < r; jj += kWarps) {
-    float* y = s.z[jj];
-    float yl[4];
+  // --- 5. back-transform: y = H_0 H_1 ... H_{n-3} z, eight reflections a block --
+  // Inside a block (reflections j0 .. j0+7, applied last first):
+  //   s_k = v_k.y - sum_{m>k} beta_m s_m (v_k.v_m),  y -= sum_k beta_k s_k v_k.
+  // Eight lanes per vector; lane q holds elements 4q + 32i + 0..3 (i < 4).
+  {
+    const int q = lane & 7;
+    for (int vec = warp * 4 + (lane >> 3); vec < r; vec += kEigThreads / 8) {
+      float y[16];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) yl[c] = y[lane + 32 * c];
-    for (int j = n - 3; j >= 0; --j) {
-      const float beta = s.beta[j];
-      if (beta == 0.f) continue;
-      const float* hv = s.hv[j];
-      float dot = 0.f;
+      for (int i = 0; i < 4; ++i) {
+        const float4 t4 = *reinterpret_cast<const float4*>(&s.z[vec][4 * q + 32 * i]);
+        y[4 * i] = t4.x; y[4 * i + 1] = t4.y; y[4 * i + 2] = t4.z; y[4 * i + 3] = t4.w;
+      }
+      const unsigned gmask = 0xffu << (lane & 24);
+#pragma unroll 1
+      for (int blk = kBtBlocks - 1; blk >= 0; --blk) {
+        const int j0 = blk * kBtBlock;
+        const int nb = min(kBtBlock, kEigSteps - j0);
+        float sdot[kBtBlock];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) dot = fmaf(hv[lane + 32 * c], yl[c], dot);
+        for (int k = 0; k < kBtBlock; ++k) {
+          float acc = 0.f;
+          if (k < nb) {
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      const float f = beta * dot;
+            for (int i = 0; i < 4; ++i) {
+              const float4 v = *reinterpret_cast<const float4*>(&s.hv[j0 + k][4 * q + 32 * i]);
+              acc = fmaf(v.x, y[4 * i], fmaf(v.y, y[4 * i + 1], fmaf(v.z, y[4 * i + 2], fmaf(v.w, y[4 * i + 3], acc))));
+            }
+          }
+          sdot[k] = acc;
+        }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) yl[c] -= f * hv[lane + 32 * c];
+        for (int o = 4; o >= 1; o >>= 1)
+#pragma unroll
+          for (int k = 0; k < kBtBlock; ++k) sdot[k] += __shfl_xor_sync(gmask, sdot[k], o);
+        float coef[kBtBlock];
+#pragma unroll
+        for (int k = kBtBlock - 1; k >= 0; --k) {
+          float sk = sdot[k];
+#pragma unroll
+          for (int m = k + 1; m < kBtBlock; ++m) sk = fmaf(-coef[m], s.vtv[blk][k][m], sk);
+          coef[k] = k < nb ? s.beta[j0 + k] * sk : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kBtBlock; ++k) {
+          if (k < nb) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 v = *reinterpret_cast<const float4*>(&s.hv[j0 + k][4 * q + 32 * i]);
+              y[4 * i] = fmaf(-coef[k], v.x, y[4 * i]);
+              y[4 * i + 1] = fmaf(-coef[k], v.y, y[4 * i + 1]);
+              y[4 * i + 2] = fmaf(-coef[k], v.z, y[4 * i + 2]);
+              y[4 * i + 3] = fmaf(-coef[k], v.w, y[4 * i + 3]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(evec_out + (size_t)vec * n + 4 * q + 32 * i) =
+            make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
     }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) y[lane + 32 * c] = yl[c];
-  }
-  __syncthreads();
-  for (int el = tid; el < kCurdkvMaxRank * n; el += kEigThreads) {
-    const int jj = el / n;
-    evec_out[el] = jj < r ? s.z[jj][el % n] : 0.f;
+    for (int el = r * n + tid; el < kCurdkvMaxRank * n; el += kEigThreads) evec_out[el] = 0.f;
   }
 }
 
 // ---------------------------------------------------------------------------
-// Leverage and cumulative score on the tensor cores. One CTA per 128 rows of
-// one (b, h): the projections P = V_tile E^T (E = the top-r eigenvectors,
-// split into bf16 hi + lo, zero rows past r) come from one M=128, N=32 MMA
-// chain with the value tile in its natural K-major layout; then
-// l_i = a_i^2 * |P_i|^2 / E, accumulated into kept rows' scores and seeding
-// incoming rows'. grid = (ceil(n / 128), B*H), block = 128.
+// Leverage and cumulative score on the tensor cores, persistent and pipelined.
+// The (b, h, 128-row tile) items of the call (kept rows from row 0, then
+// incoming rows from row k, as in the Gram kernel) are laid end to end and
+// every CTA takes an equal contiguous share. Per item, P = V_tile E^T (E = the
+// unit's top-r eigenvectors split into bf16 hi + lo, zero rows past r) comes
+// from one M = 128, N = 32 MMA chain with the value tile in its natural
+// K-major layout; then l_i = a_i^2 |P_i|^2 / E, added to kept rows' scores
+// and seeding incoming rows'.
+// Roles (192 threads): warp 0 issues the TMA loads (a ring of value tiles),
+// warp 1 the MMAs (two TMEM accumulators of 32 columns), warps 2-5 build each
+// unit's eigenvector tiles and turn accumulators into leverage, one TMEM lane
+// (one token) per thread.
 // ---------------------------------------------------------------------------
 constexpr int kEvecTileBytes = kCurdkvMaxRank * kHeadDim * 2;
-constexpr int kLevSmem = kTileBytes + 2 * kEvecTileBytes + 1024;
+constexpr int kLevStages = 4;
+constexpr int kLevThreads = 192;
+constexpr int kLevSmem = kLevStages * kTileBytes + 2 * 2 * kEvecTileBytes + 1024;
 static_assert(kCurdkvMaxRank == 32, "the leverage MMA uses N = 32");
 
-__global__ void __launch_bounds__(kAttnThreads) curdkv_leverage_kernel(const __grid_constant__ CurdkvParams p) {
+struct LevBars {
+  uint64_t v_full[kLevStages], v_empty[kLevStages];
+  uint64_t e_full[2], e_empty[2];
+  uint64_t acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+  int fail;
+};
+
+__global__ void __launch_bounds__(kLevThreads, 1) curdkv_leverage_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t bar;
-  __shared__ uint32_t tmem_base;
-  const int bh = blockIdx.y, i0 = blockIdx.x * kTile, tid = threadIdx.x, warp = tid >> 5;
+  __shared__ LevBars b;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t v_tile = tc::smem_u32(smem), ehi = v_tile + kTileBytes, elo = ehi + kEvecTileBytes;
-  const int row_end = min(p.n, i0 + kTile);
-  if (tid == 0) tc::mbar_init(&bar, 1);
-  if (warp == 0) tc::tmem_alloc(&tmem_base, kCurdkvMaxRank);
-  for (int c = tid; c < kTile * 16; c += kAttnThreads) {
-    const int r = c >> 4, j = c & 15;
-    const int row = i0 + r;
-    const bool ok = row < row_end;
-    tc::cp_async16(v_tile + tc::sw128_offset(r, j, kTile), value_row(p, bh, ok ? row : i0) + j * 16, ok ? 16u : 0u);
-  }
-  // eigenvectors -> bf16 hi and lo tiles (32 rows, K-major, swizzled)
-  const float* ev = p.evec + (size_t)bh * kCurdkvMaxRank * kHeadDim;
-  for (int item = tid; item < kCurdkvMaxRank * 16; item += kAttnThreads) {
-    const int jr = item >> 4, ch = item & 15;
-    const float4 x0 = *reinterpret_cast<const float4*>(ev + jr * kHeadDim + 8 * ch);
-    const float4 x1 = *reinterpret_cast<const float4*>(ev + jr * kHeadDim + 8 * ch + 4);
-    const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      hw[q] = pack_bf16x2(x[2 * q], x[2 * q + 1]);
-      lw[q] = pack_bf16x2(x[2 * q] - __uint_as_float(hw[q] << 16), x[2 * q + 1] - __uint_as_float(hw[q] & 0xffff0000u));
-    }
-    const uint32_t off = tc::sw128_offset(jr, ch, kCurdkvMaxRank);
-    *reinterpret_cast<uint4*>(smem + kTileBytes + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(smem + kTileBytes + kEvecTileBytes + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  }
-  tc::cp_async_wait_all();
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_base;
+  const uint32_t vring = tc::smem_u32(smem);
+  const uint32_t ering = vring + kLevStages * kTileBytes;   // unit parity u: hi at 2u, lo at 2u+1
+  const int Ck = (p.k + kTile - 1) / kTile, Cm = (p.m + kTile - 1) / kTile;
+  const int T = Ck + Cm;
+  const long long total = (long long)T * p.units;
+  const long long g0 = total * blockIdx.x / gridDim.x, g1 = total * (blockIdx.x + 1) / gridDim.x;
   if (tid == 0) {
-    constexpr uint32_t idesc = tc::idesc_bf16_f32(kTile, kCurdkvMaxRank);
-#pragma unroll
-    for (int st = 0; st < 8; ++st) {
-      const uint32_t a_off = (uint32_t)((st >> 2) * kTile * 128 + (st & 3) * 32);
-      const uint32_t b_off = (uint32_t)((st >> 2) * kCurdkvMaxRank * 128 + (st & 3) * 32);
-      const uint64_t ad = tc::sw128_desc(v_tile + a_off);
-      tc::mma_bf16(tmem, ad, tc::sw128_desc(ehi + b_off), idesc, st > 0 ? 1u : 0u);
-      tc::mma_bf16(tmem, ad, tc::sw128_desc(elo + b_off), idesc, 1u);
+    for (int i = 0; i < kLevStages; ++i) {
+      tc::mbar_init(&b.v_full[i], 1);
+      tc::mbar_init(&b.v_empty[i], 1);
     }
-    tc::mma_commit(&bar);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&b.e_full[i], 4);                  // the four epilogue warps
+      tc::mbar_init(&b.e_empty[i], 1);
+      tc::mbar_init(&b.acc_full[i], 1);
+      tc::mbar_init(&b.acc_empty[i], 4);
+    }
+    b.fail = 0;
   }
-  bool ok = false;
-  for (int spin = 0; spin < kMbarSpin && !ok; ++spin) ok = tc::mbar_try_wait(&bar, 0);
-  ok = __all_sync(0xffffffffu, ok);
-  if (!ok && (tid & 31) == 0) raise_device_error(p.err, kDevWaitTimeout);
+  if (warp == 2) tc::tmem_alloc(&b.tmem_base, 2 * kCurdkvMaxRank);
+  tc::fence_before_sync();
+  __syncthreads();
   tc::fence_after_sync();
-  const int i = i0 + tid;
-  if (ok) {
-    float proj[32];
-    tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), proj);
-    float e4[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t tmem = b.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0 && g1 > g0) {                         // TMA producer
+      tc::tma_prefetch_desc(&p.tm_vin);
+      if (Ck > 0) tc::tma_prefetch_desc(&p.tm_vst);
+      int issued[kLevStages] = {0, 0, 0, 0};
+      for (long long g = g0; g < g1; ++g) {
+        const int j = (int)(g - g0), st = j % kLevStages;
+        const int bh = (int)(g / T), i = (int)(g - (long long)bh * T);
+        if (!wait_phase(&b.v_empty[st], (uint32_t)(((j / kLevStages) & 1) ^ 1), &b.fail, p.err)) break;
+        tc::mbar_arrive_expect_tx(&b.v_full[st], (uint32_t)kTileBytes);
+        const bool kept = i < Ck;
+        const void* map = kept ? (const void*)&p.tm_vst : (const void*)&p.tm_vin;
+        const int y = kept ? kTile * i : kTile * (i - Ck);
+        for (int hf = 0; hf < 2; ++hf)
+          tc::tma_load_3d(vring + st * kTileBytes + hf * (kTileBytes / 2), map, 64 * hf, y, bh, &b.v_full[st]);
+        ++issued[st];
+      }
+      for (int i = 0; i < kLevStages; ++i)
+        if (issued[i] > 0) drain_phase(&b.v_full[i], (uint32_t)((issued[i] - 1) & 1), p.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && g1 > g0) {                         // MMA issuer
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTile, kCurdkvMaxRank);
+      int units = 0, uses[2] = {0, 0};
+      for (long long g = g0; g < g1; ++g) {
+        const int j = (int)(g - g0), st = j % kLevStages, ab = j & 1;
+        const int bh = (int)(g / T), i = (int)(g - (long long)bh * T);
+        if (g == g0 || i == 0) {                        // a new unit: its eigenvector tiles
+          if (!wait_phase(&b.e_full[units & 1], (uint32_t)((units >> 1) & 1), &b.fail, p.err)) break;
+          ++units;
+        }
+        const int ub = (units - 1) & 1;
+        if (!wait_phase(&b.v_full[st], (uint32_t)((j / kLevStages) & 1), &b.fail, p.err)) break;
+        if (!wait_phase(&b.acc_empty[ab], (uint32_t)((uses[ab] & 1) ^ 1), &b.fail, p.err)) break;
+        tc::fence_after_sync();
+        const uint32_t va = vring + st * kTileBytes, ehi = ering + 2 * ub * kEvecTileBytes, elo = ehi + kEvecTileBytes;
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) e4[jj & 3] = fmaf(proj[jj], proj[jj], e4[jj & 3]);
-    if (i < p.n) {
-      const float a = p.attn[(size_t)bh * p.rows + i];
-      const float l = a * a * ((e4[0] + e4[1]) + (e4[2] + e4[3])) * p.inv_e[bh];
-      p.lev[(size_t)bh * p.rows + i] = l;
-      if (i < p.k) p.score_st[(size_t)bh * p.cap + i] += l;
-      else p.new_score[(size_t)bh * p.new_stride + (i - p.k)] = l;
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t a_off = (uint32_t)((ks >> 2) * kTile * 128 + (ks & 3) * 32);
+          const uint32_t b_off = (uint32_t)((ks >> 2) * kCurdkvMaxRank * 128 + (ks & 3) * 32);
+          const uint64_t ad = tc::sw128_desc(va + a_off);
+          const uint32_t acc = tmem + (uint32_t)(ab * kCurdkvMaxRank);
+          tc::mma_bf16(acc, ad, tc::sw128_desc(ehi + b_off), idesc, ks > 0 ? 1u : 0u);
+          tc::mma_bf16(acc, ad, tc::sw128_desc(elo + b_off), idesc, 1u);
+        }
+        tc::mma_commit(&b.v_empty[st]);
+        tc::mma_commit(&b.acc_full[ab]);
+        ++uses[ab];
+        if (g + 1 == g1 || i == T - 1) tc::mma_commit(&b.e_empty[ub]);
+      }
+      for (int a = 0; a < 2; ++a)                       // the last MMAs finish before TMEM is released
+        if (uses[a] > 0) drain_phase(&b.acc_full[a], (uint32_t)((uses[a] - 1) & 1), p.err);
+    }
+    __syncwarp();
+  } else {                                              // epilogue: one token per thread
+    const int et = tid - 64;                            // 0 .. 127
+    const int quarter = warp & 3, row_in_tile = 32 * quarter + lane;
+    int units = 0, uses[2] = {0, 0};
+    auto attn_of = [&](long long g) -> float {
+      if (g >= g1) return 0.f;
+      const int bh = (int)(g / T), i = (int)(g - (long long)bh * T);
+      const int row = i < Ck ? kTile * i + row_in_tile : p.k + kTile * (i - Ck) + row_in_tile;
+      const int lim = i < Ck ? p.k : p.k + p.m;
+      return row < lim ? p.attn[(size_t)bh * p.rows + row] : 0.f;
+    };
+    float a_next = attn_of(g0);
+    for (long long g = g0; g < g1; ++g) {
+      const int j = (int)(g - g0), ab = j & 1;
+      const int bh = (int)(g / T), i = (int)(g - (long long)bh * T);
+      const float a_cur = a_next;
+      a_next = attn_of(g + 1);
+      if (g == g0 || i == 0) {                          // build this unit's eigenvector tiles
+        const int ub = units & 1;
+        bool ok = wait_phase(&b.e_empty[ub], (uint32_t)(((units >> 1) & 1) ^ 1), &b.fail, p.err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const float* ev = p.evec + (size_t)bh * kCurdkvMaxRank * kHeadDim;
+        unsigned char* eh = smem + kLevStages * kTileBytes + 2 * ub * kEvecTileBytes;
+        for (int item = et; item < kCurdkvMaxRank * 16; item += 128) {
+          const int jr = item >> 4, ch = item & 15;
+          const float4 x0 = *reinterpret_cast<const float4*>(ev + jr * kHeadDim + 8 * ch);
+          const float4 x1 = *reinterpret_cast<const float4*>(ev + jr * kHeadDim + 8 * ch + 4);
+          const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            hw[q] = pack_bf16x2(x[2 * q], x[2 * q + 1]);
+            lw[q] = pack_bf16x2(x[2 * q] - __uint_as_float(hw[q] << 16),
+                                x[2 * q + 1] - __uint_as_float(hw[q] & 0xffff0000u));
+          }
+          const uint32_t off = tc::sw128_offset(jr, ch, kCurdkvMaxRank);
+          *reinterpret_cast<uint4*>(eh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(eh + kEvecTileBytes + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&b.e_full[ub]);
+        ++units;
+      }
+      bool ok = wait_phase(&b.acc_full[ab], (uint32_t)(uses[ab] & 1), &b.fail, p.err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ++uses[ab];
+      tc::fence_after_sync();
+      float proj[32];
+      tc::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kCurdkvMaxRank), proj);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&b.acc_empty[ab]);
+      float e4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) e4[jj & 3] = fmaf(proj[jj], proj[jj], e4[jj & 3]);
+      const bool kept = i < Ck;
+      const int row = kept ? kTile * i + row_in_tile : p.k + kTile * (i - Ck) + row_in_tile;
+      const int lim = kept ? p.k : p.k + p.m;
+      if (row < lim) {
+        const float l = a_cur * a_cur * ((e4[0] + e4[1]) + (e4[2] + e4[3])) * p.inv_e[bh];
+        p.lev[(size_t)bh * p.rows + row] = l;
+        if (kept) p.score_st[(size_t)bh * p.cap + row] += l;
+        else p.new_score[(size_t)bh * p.new_stride + (row - p.k)] = l;
+      }
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, kCurdkvMaxRank);
+  if (warp == 2) tc::tmem_dealloc(tmem, 2 * kCurdkvMaxRank);
 }
 
 // Append the block (cache stays within budget): grid = (ceil(m / 64), B*H), block = 256.
@@ -1282,7 +1697,6 @@ void curdkv_layout(evict_handle* h, size_t* off, char* base) {
   CurdkvState& st = *h->curdkv;
   const size_t bh = (size_t)h->cfg.batch * h->cfg.n_kv_heads;
   st.rows = h->cap + h->cfg.max_block;
-  st.splits = (st.rows + kGramRows - 1) / kGramRows;
   auto take = [&](size_t bytes) {
     *off = round256(*off);
     char* p = base ? base + *off : nullptr;
@@ -1296,7 +1710,7 @@ void curdkv_layout(evict_handle* h, size_t* off, char* base) {
   st.quads = (h->cfg.max_block + kQuad * kTile - 1) / (kQuad * kTile);
   st.colpart = st.quads > 1 ? reinterpret_cast<float*>(take((size_t)st.quads * bh * st.rows * 4)) : nullptr;
   st.lev = reinterpret_cast<float*>(take(bh * st.rows * 4));
-  st.gram_part = reinterpret_cast<float*>(take(bh * st.splits * kHeadDim * kHeadDim * 4));
+  st.gram = reinterpret_cast<float*>(take(bh * kHeadDim * kHeadDim * 4));
   st.evec = reinterpret_cast<float*>(take(bh * kCurdkvMaxRank * kHeadDim * 4));
   st.inv_e = reinterpret_cast<float*>(take(bh * 4));
 }
@@ -1316,7 +1730,7 @@ int curdkv_prepare(evict_handle* h) {
                                 attn_smem_bytes(kLseStages))) != cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 attn_smem_bytes(kColStages))) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(curdkv_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramTcSmem)) !=
+      (e = cudaFuncSetAttribute(curdkv_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramSmem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_leverage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLevSmem)) !=
           cudaSuccess ||
@@ -1342,6 +1756,7 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   p.n = n;
   p.cap = h->cap;
   p.heads = c.n_kv_heads;
+  p.units = bh;
   p.rank = std::min(std::min(c.rank_cap, n), kHeadDim);
   p.scale2 = kLog2e / sqrtf((float)kHeadDim);
   p.lse = st.lse;
@@ -1350,8 +1765,7 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   p.attn = st.attn;
   p.lev = st.lev;
   p.rows = st.rows;
-  p.gram_part = st.gram_part;
-  p.splits = st.splits;
+  p.gram = st.gram;
   p.evec = st.evec;
   p.inv_e = st.inv_e;
   p.score_st = h->score_st;
@@ -1363,10 +1777,16 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   p.err = h->err;
   const cudaStream_t sm = h->stream;
   cudaError_t e;
-  const int k_tiles = (n + kTile - 1) / kTile;
   // attention passes: TMA maps of the incoming and kept keys, tile shares
   if (!encode_rows(&p.tm_kin, k, m, m, bh) || (p.k > 0 && !encode_rows(&p.tm_kst, h->kst, p.k, h->cap, bh)))
     return fail(EVICT_EINVAL, "cannot describe the key buffers for TMA (k must be 16-byte aligned)");
+  if (!encode_rows(&p.tm_vin, v, m, m, bh) || (p.k > 0 && !encode_rows(&p.tm_vst, h->vst, p.k, h->cap, bh)))
+    return fail(EVICT_EINVAL, "cannot describe the value buffers for TMA (v must be 16-byte aligned)");
+  {
+    // Gram cluster: enough CTAs per (b, h) to cover the SMs, at most one per tile and 8
+    const int tiles = (p.k + kTile - 1) / kTile + (m + kTile - 1) / kTile;
+    p.gram_cluster = std::max(1, std::min({kGramMaxCluster, st.sm_count / std::max(bh, 1), tiles}));
+  }
   p.sched1 = make_sched(p.k, m, bh, st.sm_count, true);
   p.sched2 = make_sched(p.k, m, bh, st.sm_count, false);
   p.colpart = p.sched2.Q > 1 ? st.colpart : st.attn;
@@ -1393,8 +1813,19 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV column-sum merge launch");
   }
   e = timed_launch(h, kKidCurdkvGram, [&] {
-    curdkv_gram_kernel<<<dim3((n + kGramRows - 1) / kGramRows, bh), kAttnThreads, kGramTcSmem, sm>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(p.gram_cluster * bh);
+    lc.blockDim = dim3(kGramThreads);
+    lc.dynamicSmemBytes = kGramSmem;
+    lc.stream = sm;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.gram_cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, curdkv_gram_kernel, p);
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV Gram launch");
   e = timed_launch(h, kKidCurdkvEig, [&] {
@@ -1403,7 +1834,8 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV eigensolver launch");
   e = timed_launch(h, kKidCurdkvLeverage, [&] {
-    curdkv_leverage_kernel<<<dim3(k_tiles, bh), kAttnThreads, kLevSmem, sm>>>(p);
+    const long long items = (long long)bh * ((p.k + kTile - 1) / kTile + (m + kTile - 1) / kTile);
+    curdkv_leverage_kernel<<<(int)std::min<long long>(st.sm_count, items), kLevThreads, kLevSmem, sm>>>(p);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV leverage launch");

@@ -34,6 +34,21 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor: MN-major, 128-byte swizzle. A row of the
+// swizzle atom holds 64 consecutive M (or N) elements of one K index; 8 K
+// indices form a 1024-byte atom. `mn_stride` = bytes between 64-element M/N
+// groups (leading byte offset), `k_stride` = bytes between 8-index K groups
+// (stride byte offset).
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t mn_stride, uint32_t k_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((k_stride >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
 // Instruction descriptor: kind::f16 with bf16 A and B, fp32 accumulator,
 // both operands K-major, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
@@ -42,6 +57,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
          | (1u << 10)                    // B = bf16
          | ((uint32_t)(n >> 3) << 17)    // N
          | ((uint32_t)(m >> 4) << 24);   // M
+}
+
+// The same with both operands MN-major (transposed A and B).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int m, int n) {
+  return idesc_bf16_f32(m, n) | (1u << 15) | (1u << 16);
 }
 
 // --- tensor memory ---------------------------------------------------------
@@ -155,6 +175,31 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
 }
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// --- thread-block clusters and distributed shared memory ---------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Full cluster barrier: release this thread's prior writes, acquire the others'.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(caddr)
+               : "memory");
+  return v;
 }
 
 // --- named barrier among a subset of the CTA's warps ---------------------------
