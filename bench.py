@@ -563,7 +563,11 @@ def algorithmic_work(run, binding):
                read/write its score (D*2 + 12 bytes per row).
     Flops / exponentials (CurDKV attention passes): 2*D per valid logit and
     one exponential per valid logit; L = sum over (b, h) of m*k + m(m+1)/2.
-    curdkv_gram: 2*D*D flops per row (fp32 FMA on CUDA cores).
+    curdkv_gram: 2*D*D flops per row (the bf16 hi + lo split doubles the
+               tensor-core work; the algorithmic count is one product).
+    evict1   : the fused single-eviction step: incoming keys, every row's
+               score, and the rows behind the evicted one moved down
+               (K, V, position and score read and written).
     """
     w = run.w
     e = 2 if w["dtype"] == "bf16" else 4
@@ -578,6 +582,9 @@ def algorithmic_work(run, binding):
         a, b = binding.evict_compaction_rows(h)
         old, new = old + a, new + b
     out["compact"] = {"bytes": new * (4 * 128 * e + 16) + old * (4 * 128 * e + 20)}
+    # fused single eviction: read the incoming keys and every row's score, move
+    # the rows behind the evicted one (K, V, position and score read and written)
+    out["evict1"] = {"bytes": units * m * 128 * e + units * 4 * n + new * (4 * 128 * e + 12) + old * (4 * 128 * e + 16)}
     flag_stride = -(-w["budget"] // (32 if e == 2 else 16))
     out["select"] = {"bytes": int(units * (4 * n + 4 * w["budget"] + 4 * flag_stride + 8))}
     logits = getattr(run, "logits", None)

@@ -27,6 +27,7 @@ enum KernelId : int {
   kKidCurdkvGram,
   kKidCurdkvEig,
   kKidCurdkvLeverage,
+  kKidEvict1,
   kKidCount
 };
 

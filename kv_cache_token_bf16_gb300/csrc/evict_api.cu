@@ -42,6 +42,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 const char* const kKernelNames[kKidCount] = {
     "score", "score_append", "select", "compact", "calib_gram", "calib_eig",
     "curdkv_lse", "curdkv_lse_merge", "curdkv_colsum", "curdkv_colsum_merge", "curdkv_gram", "curdkv_eig", "curdkv_leverage",
+    "evict1",
 };
 
 cudaEvent_t take_event(evict_handle* h) {
@@ -223,6 +224,14 @@ int run_intrinsic(evict_handle* const* hs, int n_layers, const void* const* k, c
       hs[l]->n_kept = (int)n;
       hs[l]->last_evicted = false;
     }
+  } else if (n == (long long)h->cfg.budget + 1 && m <= evict1_max_block()) {
+    // exactly one row leaves: fused score, selection and one-row shift
+    e = timed_launch(h, kKidEvict1, [&] { return launch_evict1(P, h->elem, h->stream); });
+    if (e != cudaSuccess) return cuda_fail(e, "single-eviction kernel launch");
+    for (int l = 0; l < n_layers; ++l) {
+      hs[l]->n_kept = h->cfg.budget;
+      hs[l]->last_evicted = true;
+    }
   } else {
     e = timed_launch(h, kKidScore, [&] { return launch_score(P, h->elem, h->stream); });
     if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
@@ -286,6 +295,7 @@ int evict_init(const evict_config* cfg, evict_handle** out) {
   };
   if ((e = cudaMemsetAsync(h->arena, 0, bytes, h->stream)) != cudaSuccess) return bail(e, "clearing the cache");
   if ((e = prepare_select()) != cudaSuccess) return bail(e, "select kernel attribute");
+  if ((e = prepare_evict1()) != cudaSuccess) return bail(e, "single-eviction kernel attribute");
   if (cfg->method == EVICT_QFILTERS) {
     const size_t fb = (size_t)cfg->n_kv_heads * kHeadDim * sizeof(float);
     if ((e = cudaMemcpyAsync(h->filters, cfg->filters, fb, cudaMemcpyDeviceToDevice, h->stream)) != cudaSuccess)

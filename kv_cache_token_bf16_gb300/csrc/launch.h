@@ -20,5 +20,11 @@ cudaError_t prepare_select();
 cudaError_t launch_select(const GroupParams& P, cudaStream_t st);
 // Sets P.total_ctas.
 cudaError_t launch_compact(GroupParams& P, int dtype_bytes, cudaStream_t st);
+// Fused score + single eviction + one-row shift (the concatenation exceeds the
+// budget by exactly one row and m <= evict1_max_block()).
+int evict1_max_block();
+// Raise the single-eviction kernel's dynamic shared memory limit (current device).
+cudaError_t prepare_evict1();
+cudaError_t launch_evict1(const GroupParams& P, int dtype_bytes, cudaStream_t st);
 
 }  // namespace evict

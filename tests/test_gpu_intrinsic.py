@@ -116,6 +116,45 @@ def test_ties_nan_signed_zero_and_infinity(method):
     _feed(gpu, ref, k, v, [0, 400, 401, 700], check_each=True, what="ties")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("method,extra", [("knorm", {"keep_low": True}), ("knorm", {"keep_low": False}),
+                                          ("qfilters", {"sign": -1})])
+def test_single_eviction_blocks(dtype, method, extra):
+    """Blocks that overshoot the budget by exactly one row take the fused
+    single-eviction kernel (m <= 64); m = 65 takes the general path. Both
+    must give the oracle's cache bit for bit."""
+    from kv_cache_token_bf16_gb300 import binding
+    B, H, budget = 2, 3, 96
+    k, v = synth.gaussian_block(501, B, H, 400, dtype=dtype, scale=2.0)
+    kw = dict(n_sink=4, recent=6, **extra)
+    if method == "qfilters":
+        kw["filters"] = synth.unit_vectors(synth.rng(19), H).astype(np.float32)
+    for cuts in ([0, 90, 97, 98, 99, 163, 164], [0, 33, 97, 98], [0, 32, 97, 98]):
+        gpu, ref = _pair(method, B, H, budget, dtype=dtype, max_block=128, **kw)
+        binding.evict_set_profiling(gpu.handle, True)
+        _feed(gpu, ref, k, v, cuts, check_each=True, what=f"{method} {dtype} {cuts}")
+        used = binding.evict_kernel_times(gpu.handle)
+        assert "evict1" in used                           # the m <= 64 single evictions
+        assert gpu.stats() == ref.stats()
+        gpu.close()
+
+
+@pytest.mark.parametrize("method", ["knorm", "qfilters"])
+def test_single_eviction_ties_and_nan(method):
+    """All-equal keys evict the highest unprotected index; a NaN score is evicted first."""
+    B, H, budget = 1, 2, 40
+    g = synth.rng(31)
+    key = synth.f32_to_bf16_bits(g.standard_normal(128).astype(np.float32))
+    k = np.broadcast_to(key, (B, H, 60, 128)).copy()
+    k[0, 1, 45, 9] = 0x7FC0                               # NaN in the row that arrives at step 45
+    v = synth.f32_to_bf16_bits(g.standard_normal((B, H, 60, 128)).astype(np.float32))
+    kw = dict(n_sink=2, recent=3)
+    if method == "qfilters":
+        kw.update(filters=synth.unit_vectors(synth.rng(3), H).astype(np.float32), sign=1)
+    gpu, ref = _pair(method, B, H, budget, max_block=64, **kw)
+    _feed(gpu, ref, k, v, [0] + list(range(budget, 61)), check_each=True, what="single-eviction ties")
+
+
 def test_all_scores_equal_keeps_exactly_budget_lowest_indices():
     B, H, S = 1, 4, 500
     row = synth.f32_to_bf16_bits(np.linspace(-1, 1, 128, dtype=np.float32))
