@@ -58,6 +58,7 @@ struct evict_handle {
   int32_t* src_map = nullptr;
   int2* meta = nullptr;
   int* flags = nullptr;
+  int2* waits = nullptr;
   int* err = nullptr;
   void* k_stage = nullptr;
   void* v_stage = nullptr;

@@ -15,19 +15,21 @@ namespace {
 // Destination rows are cut into chunks of kChunk rows; a CTA moves one chunk
 // of one (layer, b, h). Every survivor moves to a destination at or below
 // its source, so a chunk's writes can only clobber storage rows that LOWER
-// chunks still have to read. Each CTA therefore
+// chunks still have to read. With kept rows before the call (k > 0) each CTA
 //   (1) takes the next chunk index of its (layer, b, h) from a per-unit
 //       counter, so a lower chunk always belongs to a CTA that is already
 //       running (every wait below ends);
 //   (2) loads its sources into registers and proves the loads complete by
 //       consuming them (an XOR into shared memory) before a barrier;
 //   (3) publishes a read-done flag (release) and waits (acquire, bounded)
-//       only for the lower chunks whose kept-row sources overlap its
-//       destinations;
+//       for the lower chunks whose kept-row sources lie in its destinations
+//       (a range the select kernel recorded per chunk);
 //   (4) stores.
 // Rows below the first eviction never move and are not touched. Incoming
-// survivors are read straight from the caller's K/V blocks. The counter is
-// the last slot of the unit's flag array; the select kernel zeroes both.
+// survivors are read straight from the caller's K/V blocks, so with no kept
+// rows (k = 0) nothing can be clobbered: the chunk is the CTA's own and no
+// counter, flag or wait is used. The counter is the last slot of the unit's
+// flag array; the select kernel zeroes both.
 // ---------------------------------------------------------------------------
 constexpr int kCompactThreads = 256;
 
@@ -37,6 +39,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
   constexpr int kPer = kChunk * kVpr / kCompactThreads;      // vectors per thread (K and V each)
   static_assert(kChunk * kVpr % kCompactThreads == 0, "chunk must split evenly over the CTA");
   __shared__ int s_chunk, s_abort;
+  __shared__ int2 s_wait;
   __shared__ volatile uint32_t s_sink[kCompactThreads];
   const Shape& s = P.s;
   const int tid = threadIdx.x;
@@ -47,8 +50,9 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
   const int bh = u % bhn, b = bh / s.heads;
   int* flags = L.flags + (size_t)bh * s.flag_stride;
   const int chunks = s.flag_stride - 1;
+  const bool ordered = s.k > 0;                              // kept rows can be clobbered
   if (tid == 0) {
-    s_chunk = atomicAdd(&flags[chunks], 1);                  // per-unit chunk counter
+    s_chunk = ordered ? atomicAdd(&flags[chunks], 1) : (int)(blockIdx.x / units);   // per-unit chunk counter
     s_abort = 0;
   }
   __syncthreads();
@@ -57,12 +61,17 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
     if (tid == 0) raise_device_error(P.err, kDevBadIndex);
     return;
   }
-  const int2 meta = L.meta[bh];
-  const int first = meta.x, old_kept = meta.y;
+  if (tid == 0 && ordered) s_wait = L.waits[(size_t)bh * chunks + c];   // lower chunks to wait for
+  int first = 0, old_kept = 0;
+  if (ordered) {
+    const int2 meta = L.meta[bh];
+    first = meta.x;
+    old_kept = meta.y;
+  }
   const int d_lo = max(c * kChunk, first);
   const int d_hi = min(c * kChunk + kChunk, s.budget);
   if (d_lo >= d_hi) {
-    if (tid == 0) st_release(&flags[c], 1);
+    if (tid == 0 && ordered) st_release(&flags[c], 1);
     return;
   }
   const int32_t* src = L.src_map + (size_t)bh * s.cap;
@@ -117,18 +126,12 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
   if (bad) s_abort = 1;
   __syncthreads();
 
-  // (3) publish, then wait for overlapping lower chunks
-  if (tid == 0) {
-    __threadfence();
+  // (3) publish, then wait for the lower chunks that read our destinations
+  if (tid == 0 && ordered) {
     st_release(&flags[c], 1);
     if (!s_abort) {
-      for (int j = c - 1; j >= 0; --j) {
-        if (j * kChunk + kChunk <= first) break;             // this and all lower chunks read nothing
-        const int j_lo = max(j * kChunk, first);
-        const int j_hi = min(j * kChunk + kChunk, old_kept); // kept-row-sourced destinations of chunk j
-        if (j_lo >= j_hi) continue;                          // chunk j reads only incoming rows
-        if (src[j_hi - 1] < d_lo) break;                     // chunk j (and lower) read below our range
-        if (src[j_lo] >= d_hi) continue;                     // chunk j reads above our range
+      const int2 w = s_wait;
+      for (int j = w.x; j <= w.y && j < c; ++j) {
         int spins = 0;
         while (ld_acquire(&flags[j]) == 0) {
           if (++spins > kSpinLimit) {
@@ -143,6 +146,8 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
     } else {
       raise_device_error(P.err, kDevBadIndex);
     }
+  } else if (tid == 0 && s_abort) {
+    raise_device_error(P.err, kDevBadIndex);
   }
   __syncthreads();
   if (s_abort) return;

@@ -102,6 +102,7 @@ size_t arena_layout(evict_handle* h, char* base) {
   h->src_map = cv.take<int32_t>(bh * h->cap * 4);
   h->meta = cv.take<int2>(bh * sizeof(int2));
   h->flags = cv.take<int>(bh * h->flag_stride * 4);
+  h->waits = cv.take<int2>(bh * (h->flag_stride - 1) * sizeof(int2));
   h->err = cv.take<int>(4);
   h->k_stage = cv.take<void>(bh * c.max_block * kHeadDim * e);
   h->v_stage = cv.take<void>(bh * c.max_block * kHeadDim * e);
@@ -161,6 +162,7 @@ GroupParams make_group_params(const evict_handle* h, int m, int n_layers) {
   P.s.recent = c.recent;
   P.s.new_stride = h->new_stride;
   P.s.flag_stride = h->flag_stride;
+  P.s.chunk = h->chunk;
   P.s.n_layers = n_layers;
   P.s.keep_low = c.method == EVICT_KNORM ? c.keep_low : 0;
   P.s.sign = (float)(c.method == EVICT_QFILTERS ? c.sign : 1);
@@ -184,6 +186,7 @@ LayerPtrs make_layer_ptrs(evict_handle* h, const void* k, const void* v, const i
   L.src_map = h->src_map;
   L.meta = h->meta;
   L.flags = h->flags;
+  L.waits = h->waits;
   return L;
 }
 

@@ -125,6 +125,7 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
   P.s.recent = c.recent;
   P.s.new_stride = n;
   P.s.flag_stride = flag_stride;
+  P.s.chunk = compact_chunk_rows(elem);
   P.s.n_layers = 1;
   P.s.keep_low = c.method == EVICT_KNORM ? c.keep_low : 0;
   P.s.sign = (float)(c.method == EVICT_QFILTERS ? c.sign : 1);

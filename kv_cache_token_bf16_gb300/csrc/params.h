@@ -25,6 +25,9 @@ struct LayerPtrs {
   int32_t* src_map;        // [B, H, cap] source row of each kept destination
   int2* meta;              // [B, H] {first moved destination, old survivors}
   int* flags;              // [B, H, flag_stride] compaction read-done flags, then the chunk counter
+  int2* waits;             // [B, H, flag_stride - 1] per destination chunk, the lower chunks whose
+                           // reads of kept rows overlap its destinations ({lo, hi}; empty: hi < lo);
+                           // written by the select kernel when k > 0
 };
 
 // Sizes common to every layer of a grouped update.
@@ -37,6 +40,7 @@ struct Shape {
   int n_sink, recent;
   int new_stride;          // row stride of new_score (max_block)
   int flag_stride;         // flag slots per (b, h): one per chunk + the chunk counter
+  int chunk;               // rows per compaction chunk
   int n_layers;
   int keep_low;            // KNorm keep-low: priority = -score
   float sign;              // Q-Filters sign

@@ -63,6 +63,28 @@ __device__ __forceinline__ uint32_t block_excl_sum(uint32_t x, uint32_t* scratch
 // ---------------------------------------------------------------------------
 constexpr int kDigitBits = 11;
 constexpr int kBins = 1 << kDigitBits;
+// destination chunks per (b, h) the wait ranges can describe (smallest chunk: 32 rows)
+constexpr int kMaxWaitChunks = (EVICT_MAX_SELECT_ROWS + 31) / 32;
+
+// Wait ranges of the compaction: a survivor with destination d and kept
+// source sr (sr < k) is read by chunk d / C and overwritten by chunk sr / C;
+// when those differ the overwriting chunk must wait for the reading one.
+__device__ __forceinline__ void note_wait(int* wlo, int* whi, int d, int sr, int chunk) {
+  const int cd = d / chunk, cs = sr / chunk;
+  if (cd < cs) {
+    atomicMin(&wlo[cs], cd);
+    atomicMax(&whi[cs], cd);
+  }
+}
+__device__ __forceinline__ void init_waits(int* wlo, int* whi, int chunks) {
+  for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+    wlo[c] = 0x7fffffff;
+    whi[c] = -1;
+  }
+}
+__device__ __forceinline__ void store_waits(const int* wlo, const int* whi, int2* out, int chunks) {
+  for (int c = threadIdx.x; c < chunks; c += blockDim.x) out[c] = make_int2(wlo[c], whi[c]);
+}
 
 template <int kThreads, int kPer>
 __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant__ GroupParams P) {
@@ -71,6 +93,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
   __shared__ uint32_t s_min[32], s_max[32];
   __shared__ uint32_t s_prefix, s_rem;
   __shared__ int s_first, s_old_kept;
+  __shared__ int s_wlo[kMaxWaitChunks], s_whi[kMaxWaitChunks];
   const Shape& s = P.s;
   const int bhn = s.batch * s.heads;
   const int u = blockIdx.x;
@@ -78,6 +101,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
   const int bh = u % bhn;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kWarps = kThreads / 32;
+  const int chunks = s.flag_stride - 1;
+  if (s.k > 0) init_waits(s_wlo, s_whi, chunks);
   const int n = s.k + s.m;
   const int lo = s.n_sink, hi = n - s.recent;
   const int q = s.budget - (n - (hi - lo));      // unprotected rows to keep (>= 1)
@@ -204,8 +229,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
     if (keep_bits & (1u << j)) {
       if (dest < (uint32_t)s.budget) src_map[dest] = i;
       else raise_device_error(P.err, kDevBadIndex);
+      if (i < s.k) {
+        ++old_kept;
+        note_wait(s_wlo, s_whi, (int)dest, i, s.chunk);
+      }
       ++dest;
-      if (i < s.k) ++old_kept;
     } else if (i < s.k && i < first_drop) {
       first_drop = i;
     }
@@ -215,6 +243,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
   if (lane == 0 && wsum) atomicAdd(&s_old_kept, (int)wsum);
   __syncthreads();
   if (tid == 0) L.meta[bh] = make_int2(s_first, s_old_kept);
+  if (s.k > 0) store_waits(s_wlo, s_whi, L.waits + (size_t)bh * chunks, chunks);
 }
 
 // ---------------------------------------------------------------------------
@@ -236,6 +265,7 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
   __shared__ uint32_t scan[65];
   __shared__ uint32_t s_prefix, s_rem;
   __shared__ int s_first, s_old_kept;
+  __shared__ int s_wlo[kMaxWaitChunks], s_whi[kMaxWaitChunks];
   const Shape& s = P.s;
   const int bhn = s.batch * s.heads;
   const int u = blockIdx.x;
@@ -243,6 +273,8 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
   const int bh = u % bhn;
   const int tid = threadIdx.x, lane = tid & 31;
   const int n = s.k + s.m;
+  const int chunks = s.flag_stride - 1;
+  if (s.k > 0) init_waits(s_wlo, s_whi, chunks);
   const float* old_score = L.score_st + (size_t)bh * s.cap;
   const float* new_score = L.new_score + (size_t)bh * s.new_stride;
   for (int i = tid; i < n; i += kThreads) {
@@ -341,8 +373,11 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
       if (keep) {
         if (dest < (uint32_t)s.budget) src_map[dest] = i;
         else raise_device_error(P.err, kDevBadIndex);
+        if (i < s.k) {
+          ++old_kept;
+          note_wait(s_wlo, s_whi, (int)dest, i, s.chunk);
+        }
         ++dest;
-        if (i < s.k) ++old_kept;
       } else if (i < s.k && i < first_drop) {
         first_drop = i;
       }
@@ -353,6 +388,7 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
   if (lane == 0 && wsum) atomicAdd(&s_old_kept, (int)wsum);
   __syncthreads();
   if (tid == 0) L.meta[bh] = make_int2(s_first, s_old_kept);
+  if (s.k > 0) store_waits(s_wlo, s_whi, L.waits + (size_t)bh * chunks, chunks);
 }
 
 template <typename Kernel>
