@@ -24,12 +24,24 @@ their storage format (plus, for Q-Filters, the frozen filter: D * 4 bytes
 per KV head); full_seq_bytes is the cost had every token been kept;
 compression_ratio = full_seq_bytes / kept_bytes.
 
+Key-SVD fallback ("Q-Filters", §How it works step 2, §Key-SVD fallback,
+§Path dependence): Q-Filters without calibrated filters keeps every row
+(no filter, so no eviction, even over budget) while the keys seen stay below
+calib_tokens. The call whose block reaches calib_tokens estimates, per
+(b, h), the filter from all keys present then (calibrate.key_svd_filter),
+freezes it, scores every stored row once with it, and evicts as usual.
+Which keys are present at that call depends on the chunking, which is the
+path dependence the page describes. Reading: each (b, h) freezes its own
+filter (the page's per-group filter freezing) and the byte accounting
+counts those filters (D * 4 bytes per (b, h)) once frozen.
+
 Build-time validation ("Q-Filters", §Evidence: n_sink + recent >= budget
 and an invalid sign raise; filters whose head layout disagrees with the
 layer raise).
 """
 import numpy as np
 
+from . import calibrate as _calibrate
 from . import curdkv as _curdkv
 from . import scores as _scores
 from .bf16 import to_f64
@@ -40,7 +52,8 @@ KNORM, QFILTERS, CURDKV = "knorm", "qfilters", "curdkv"
 
 class OracleCache:
     def __init__(self, method, batch, n_kv_heads, budget, n_sink=4, recent=0, keep_low=True,
-                 sign=1, filters=None, rank_cap=16, head_dim=128, dtype="bf16", score_mode="canonical"):
+                 sign=1, filters=None, rank_cap=16, head_dim=128, dtype="bf16", score_mode="canonical",
+                 calib_tokens=128, filter_override=None):
         if method not in (KNORM, QFILTERS, CURDKV):
             raise ValueError(f"unknown method {method}")
         if n_sink < 0 or recent < 0 or budget <= 0:
@@ -49,12 +62,13 @@ class OracleCache:
             raise ValueError("n_sink + recent must be below the budget")
         if sign not in (1, -1):
             raise ValueError("sign must be +1 or -1")
-        if method == QFILTERS:
-            if filters is None:
-                raise ValueError("calibrated Q-Filters needs filters")
+        self.fallback = method == QFILTERS and filters is None
+        if method == QFILTERS and not self.fallback:
             filters = np.asarray(filters, dtype=np.float32)
             if filters.shape != (n_kv_heads, head_dim):
                 raise ValueError("filter head layout does not match the layer")
+        if self.fallback and calib_tokens < 1:
+            raise ValueError("calib_tokens must be >= 1")
         if method == CURDKV and rank_cap <= 0:
             raise ValueError("rank_cap must be positive")
         self.method, self.batch, self.heads, self.d = method, batch, n_kv_heads, head_dim
@@ -70,6 +84,9 @@ class OracleCache:
         self.offset = 0
         self.last_kept = None          # indices kept by the last call, [B, H, n_kept]
         self.last_leverage = None      # CurDKV: leverage of the last call's rows
+        self.calib_tokens = calib_tokens
+        self.filter_override = filter_override   # tests: (b, h) -> fp32 filter used at the freeze
+        self.filters_bh = None         # fallback: frozen per-(b, h) filters [B, H, D] fp32
 
     # ------------------------------------------------------------------
     def set_state(self, k, v, pos, score, offset):
@@ -83,7 +100,25 @@ class OracleCache:
     def n_kept(self) -> int:
         return self.k.shape[2]
 
+    def _project(self, k, filters_bh):
+        """Canonical fp32 projection of k [B, H, n, D] onto per-(b, h) filters."""
+        return np.concatenate([_scores.projection_canonical(k[b:b + 1], filters_bh[b], self.sign)
+                               for b in range(self.batch)], axis=0)
+
+    def _freeze(self, k_all):
+        """Fallback: estimate and freeze every (b, h)'s filter from the keys present."""
+        f = np.empty((self.batch, self.heads, self.d), np.float32)
+        for b in range(self.batch):
+            for h in range(self.heads):
+                if self.filter_override is not None:
+                    f[b, h] = np.asarray(self.filter_override(b, h), np.float32)
+                else:
+                    f[b, h] = _calibrate.key_svd_filter(k_all[b, h]).astype(np.float32)
+        self.filters_bh = f
+
     def _score_new(self, k_new):
+        if self.fallback:
+            return self._project(k_new, self.filters_bh)
         if self.method == KNORM:
             if self.score_mode == "canonical":
                 return _scores.key_norm_canonical(k_new)
@@ -114,6 +149,17 @@ class OracleCache:
                     self.last_leverage[b, h] = l
                     score_all[b, h] = _curdkv.cumulative(self.score[b, h], l)
             prio = priority(score_all, keep_low=False)
+        elif self.fallback and self.filters_bh is None:
+            if self.offset + m < self.calib_tokens:
+                # no filter yet: keep everything (placeholder scores, replaced at the freeze)
+                self.k, self.v, self.pos = k_all, v_all, pos_all
+                self.score = np.zeros(k_all.shape[:3], np.float32)
+                self.last_kept = np.broadcast_to(np.arange(k_all.shape[2]), k_all.shape[:3])
+                self.offset += m
+                return self.k, self.v, self.pos, self.score
+            self._freeze(k_all)
+            score_all = self._project(k_all, self.filters_bh)
+            prio = priority(score_all, keep_low=False)
         else:
             score_all = np.concatenate([self.score, self._score_new(k_new).astype(self.score.dtype)], axis=2)
             prio = priority(score_all, keep_low=(self.method == KNORM and self.keep_low))
@@ -129,8 +175,10 @@ class OracleCache:
         e = self.k.dtype.itemsize
         per_token = self.batch * self.heads * 2 * self.d * e
         kept = per_token * self.n_kept
-        if self.method == QFILTERS:
+        if self.method == QFILTERS and not self.fallback:
             kept += self.heads * self.d * 4
+        elif self.fallback and self.filters_bh is not None:
+            kept += self.batch * self.heads * self.d * 4
         full = per_token * self.offset
         return {
             "tokens_seen": self.offset,

@@ -9,6 +9,13 @@ singular vector v1 and fix its sign as sgn(1^T u1) * v1; under GQA, average
 the filters of each query-head group onto its KV head. §Evidence: GQA
 averaging keeps the filters unit-norm.
 
+Key-SVD fallback ("Q-Filters", §Calibrated vs key-SVD fallback and §Key-SVD
+fallback): with no calibrated filter, the filter is the top right singular
+vector of the MEAN-CENTRED keys observed so far, frozen once estimated. The
+pages say the sign is ambiguous; reading: the component of largest magnitude
+is made positive (the lowest index on ties), and the configured sign is
+applied on top.
+
 Readings:
 * sgn(0) is taken as +1.
 * Query head h belongs to KV head h // G with G = H_q / H_kv (contiguous
@@ -56,3 +63,17 @@ def centered_top_direction(q: np.ndarray) -> np.ndarray:
     x = x - x.mean(axis=0, keepdims=True)
     _, _, vt = np.linalg.svd(x, full_matrices=False)
     return vt[0]
+
+
+def key_svd_filter(keys: np.ndarray) -> np.ndarray:
+    """Key-SVD fallback filter of one (b, h): keys [n, D] -> unit direction (fp64).
+
+    Top right singular vector of the mean-centred keys; the largest-magnitude
+    component is made positive (the first one on ties).
+    """
+    x = to_f64(keys)
+    x = x - x.mean(axis=0, keepdims=True)
+    _, _, vt = np.linalg.svd(x, full_matrices=False)
+    v = vt[0]
+    j = int(np.argmax(np.abs(v)))
+    return v if v[j] >= 0 else -v

@@ -139,5 +139,5 @@ def test_invalid_configs_raise(kw):
 def test_filter_head_layout_mismatch_raises():
     with pytest.raises(ValueError):
         OracleCache("qfilters", 1, 8, budget=64, filters=np.zeros((4, 128), np.float32))
-    with pytest.raises(ValueError):
-        OracleCache("qfilters", 1, 8, budget=64, filters=None)
+    with pytest.raises(ValueError):      # filters=None is the key-SVD fallback; it needs calib_tokens >= 1
+        OracleCache("qfilters", 1, 8, budget=64, filters=None, calib_tokens=0)
