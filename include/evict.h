@@ -75,13 +75,27 @@ typedef struct evict_config {
                           0 the highest ("L2Norm", §Usage, knorm_keep) */
   int sign;            /* Q-Filters: +1 or -1 ("Q-Filters", §Usage, qfilters_sign) */
   const float* filters;/* Q-Filters: device [n_filter_heads, head_dim] fp32 unit filters,
-                          COPIED at init and frozen ("Q-Filters", §How it works step 3) */
+                          COPIED at init and frozen ("Q-Filters", §How it works step 3).
+                          NULL selects the key-SVD fallback (see calib_tokens). */
   int n_filter_heads;  /* Q-Filters: rows of `filters`; must equal n_kv_heads (0 = assume
                           equal). A mismatch raises ("Q-Filters", §Evidence: filters whose
                           head layout disagrees with the layer raise). */
   int rank_cap;        /* CurDKV: leading singular directions (default 16 when 0;
                           "CurDKV-adapted", §Usage, curdkv_rank_cap) */
   void* stream;        /* cudaStream_t for all work of this handle (NULL = legacy default) */
+  int calib_tokens;    /* Q-Filters key-SVD fallback (filters == NULL) only: keys seen before
+                          the filters freeze (0 = default 128; "Q-Filters", §Usage,
+                          qfilters_calib_tokens). While offset + m < calib_tokens an update
+                          keeps every row, even over budget, with score 0 (no filter, no
+                          eviction). The update that reaches calib_tokens freezes, per
+                          (b, h), the top right singular vector of the mean-centred keys
+                          present then (kept rows and block), its largest-magnitude
+                          component made positive (e_0 when every key is equal), re-scores
+                          the kept rows with it and evicts as usual (§How it works step 2,
+                          §Key-SVD fallback, §Path dependence: the frozen direction depends
+                          on the chunking). Capacity is at least calib_tokens - 1 rows.
+                          A non-finite key Gram at the freeze is reported by evict_sync
+                          as EVICT_EDEVICE. evict_reset unfreezes. Ignored otherwise. */
 } evict_config;
 
 /* The kept cache after a call. Pointers are library-owned device memory,
@@ -105,7 +119,8 @@ typedef struct evict_view {
 typedef struct evict_stats_t {
   int64_t tokens_seen;       /* = offset: absolute tokens passed to updates */
   int64_t tokens_kept;       /* rows per (b,h) */
-  int64_t kept_bytes;        /* B*H*tokens_kept*2*D*elem (+ H*D*4 for Q-Filters' filter) */
+  int64_t kept_bytes;        /* B*H*tokens_kept*2*D*elem (+ H*D*4 for Q-Filters' filters;
+                                the key-SVD fallback counts B*H*D*4 once frozen) */
   int64_t full_seq_bytes;    /* B*H*tokens_seen*2*D*elem */
   double compression_ratio;  /* full_seq_bytes / kept_bytes (0 when nothing kept) */
   int64_t offset;            /* true absolute position of the next token */
@@ -241,6 +256,12 @@ int evict_kernel_times(evict_handle* h, evict_kernel_time* out, int max_entries,
  * count the compaction's algorithmic bytes). Both are 0 if the last update
  * appended without eviction. */
 int evict_compaction_rows(evict_handle* h, int64_t* old_moved, int64_t* new_written);
+
+/* Q-Filters: copy the filters in use to the HOST buffer out_host (may be
+ * NULL to query only) and set *n_rows: n_kv_heads rows [H, D] for calibrated
+ * filters, B*H rows [B, H, D] once the key-SVD fallback has frozen, 0 before
+ * (nothing copied). Synchronises the stream. EVICT_EINVAL for other methods. */
+int evict_qfilters_filters(evict_handle* h, float* out_host, int* n_rows);
 
 /* CurDKV diagnostics: copy the last update's proxy-attention column sums
  * and leverage of every row of the concatenation (kept rows first, then the

@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libevict.so")
 
 SOURCES = ["score_kernels.cu", "select_kernel.cu", "compact_kernel.cu", "evict_api.cu", "calib.cu", "curdkv.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "fallback.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

@@ -32,7 +32,7 @@ class EvictConfig(ctypes.Structure):
         ("n_sink", ctypes.c_int), ("recent", ctypes.c_int), ("max_block", ctypes.c_int),
         ("max_kept", ctypes.c_int), ("keep_low", ctypes.c_int), ("sign", ctypes.c_int),
         ("filters", ctypes.c_void_p), ("n_filter_heads", ctypes.c_int), ("rank_cap", ctypes.c_int),
-        ("stream", ctypes.c_void_p),
+        ("stream", ctypes.c_void_p), ("calib_tokens", ctypes.c_int),
     ]
 
 
@@ -80,6 +80,7 @@ _SIGNATURES = {
     "evict_compaction_rows": (_I, [_P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "evict_prefill_noalloc": (_I, [ctypes.POINTER(EvictConfig), _P, _P, _P, _I, _P, _P, _P, _P]),
     "evict_curdkv_scores": (_I, [_P, _P, _P, ctypes.POINTER(_I)]),
+    "evict_qfilters_filters": (_I, [_P, _P, ctypes.POINTER(_I)]),
     "evict_launch_count": (ctypes.c_int64, []),
     "evict_last_error": (ctypes.c_char_p, []),
 }
@@ -207,6 +208,17 @@ def evict_curdkv_scores(h, attn_ptr, lev_ptr) -> int:
     return n.value
 
 
+def evict_qfilters_filters(h):
+    """Filters in use as a numpy fp32 array [rows, 128] (rows = 0 before a fallback freeze)."""
+    import numpy as np
+    n = _I()
+    check(load().evict_qfilters_filters(h, None, ctypes.byref(n)))
+    out = np.zeros((n.value, HEAD_DIM), np.float32)
+    if n.value:
+        check(load().evict_qfilters_filters(h, out.ctypes.data, ctypes.byref(n)))
+    return out
+
+
 def evict_launch_count() -> int:
     return load().evict_launch_count()
 
@@ -249,16 +261,17 @@ class EvictCache:
 
     def __init__(self, method: str, batch: int, n_kv_heads: int, budget: int, n_sink: int = 4, recent: int = 0,
                  max_block: int = 8192, max_kept: int = 0, keep_low: bool = True, sign: int = 1, filters=None,
-                 rank_cap: int = 16, dtype: str = "bf16", stream=None):
+                 rank_cap: int = 16, dtype: str = "bf16", stream=None, calib_tokens: int = 128):
         import torch
         self.method, self.batch, self.heads, self.dtype = method, batch, n_kv_heads, dtype
+        self._fallback = method == "qfilters" and filters is None
         if stream is None:
             stream = torch.cuda.current_stream().cuda_stream
         self._filters = None
         cfg = EvictConfig(method=METHODS[method], dtype=DTYPES[dtype], batch=batch, n_kv_heads=n_kv_heads,
                           head_dim=HEAD_DIM, budget=budget, n_sink=n_sink, recent=recent, max_block=max_block,
                           max_kept=max_kept, keep_low=int(keep_low), sign=sign, filters=None,
-                          n_filter_heads=0, rank_cap=rank_cap, stream=stream)
+                          n_filter_heads=0, rank_cap=rank_cap, stream=stream, calib_tokens=calib_tokens)
         if filters is not None:
             f = torch.as_tensor(filters, dtype=torch.float32).cuda().contiguous()
             if f.dim() != 2 or f.shape[1] != HEAD_DIM:
@@ -305,3 +318,11 @@ class EvictCache:
 
     def stats(self):
         return evict_stats(self.handle)
+
+    def filters(self):
+        """Q-Filters: the filters in use, numpy [H, 128] calibrated or [B, H, 128] once the
+        key-SVD fallback has frozen (None before)."""
+        f = evict_qfilters_filters(self.handle)
+        if f.shape[0] == 0:
+            return None
+        return f if f.shape[0] == self.heads and not self._fallback else f.reshape(self.batch, self.heads, HEAD_DIM)

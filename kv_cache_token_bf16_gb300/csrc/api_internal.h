@@ -28,6 +28,7 @@ enum KernelId : int {
   kKidCurdkvEig,
   kKidCurdkvLeverage,
   kKidEvict1,
+  kKidFreeze,
   kKidCount
 };
 
@@ -45,6 +46,8 @@ struct evict_handle {
   int chunk = 64;             // compaction chunk rows
   int flag_stride = 0;        // compaction flag slots per (b, h): chunk flags + chunk counter
   int new_stride = 0;         // row stride of new_score (= max_block)
+  bool fallback = false;      // Q-Filters without calibrated filters: key-SVD fallback
+  bool frozen = false;        // fallback: the per-(b, h) filters have been estimated
   cudaStream_t stream = nullptr;
 
   void* arena = nullptr;      // one device allocation, carved below
@@ -53,7 +56,7 @@ struct evict_handle {
   void* vst = nullptr;
   int32_t* pos_st = nullptr;
   float* score_st = nullptr;
-  float* filters = nullptr;
+  float* filters = nullptr;   // [H, D] calibrated, or [B, H, D] for the fallback
   float* new_score = nullptr;
   int32_t* src_map = nullptr;
   int2* meta = nullptr;

@@ -20,15 +20,15 @@
 
 #include "api_internal.h"
 #include "common.cuh"
+#include "power.cuh"
 
 namespace evict {
 namespace {
 
 constexpr int kGramThreads = 256;
 constexpr int kGramTileRows = 32;
-constexpr int kEigThreads = 256;
-constexpr int kCStride = kHeadDim + 1;      // padded row stride of C in shared memory
-constexpr int kMaxPowerIters = 20000;
+constexpr int kEigThreads = kPowerThreads;
+constexpr int kCStride = kPowerStride;
 
 enum CalibStatus : int { kCalibOk = 0, kCalibZeroHead = 1, kCalibDegenerateGroup = 2 };
 
@@ -120,44 +120,7 @@ calib_eig_kernel(const float* part_c, const float* part_sum, int splits, float* 
   }
   if (tid < kHeadDim) v[tid] = c[tid * kCStride + s_col] / s_norm;
   __syncthreads();
-  const int row = tid >> 1, half = tid & 1;
-  for (int it = 0; it < kMaxPowerIters; ++it) {
-    float acc = 0.f;
-    const float* cr = c + row * kCStride + half * 64;
-    const float* vv = v + half * 64;
-#pragma unroll 8
-    for (int j = 0; j < 64; ++j) acc = fmaf(cr[j], vv[j], acc);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    if (half == 0) w[row] = acc;
-    __syncthreads();
-    if (tid < 32) {
-      float ss = 0.f;
-      for (int i = lane; i < kHeadDim; i += 32) ss += w[i] * w[i];
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) s_norm = sqrtf(ss);
-    }
-    __syncthreads();
-    float d = 0.f;
-    if (tid < kHeadDim) {
-      const float nv = w[tid] / s_norm;
-      d = (nv - v[tid]) * (nv - v[tid]);
-      v[tid] = nv;
-    }
-    if ((it & 15) != 15) {
-      __syncthreads();
-      continue;
-    }
-    if (tid == 0) s_delta = 0.f;
-    __syncthreads();
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-    if (lane == 0 && tid < kHeadDim) atomicAdd(&s_delta, d);
-    __syncthreads();
-    // Stop once the unit iterate moves by less than 3e-6 over one iteration:
-    // a few times the fp32 rounding floor of a 128-long matvec.
-    if (s_delta < 1e-11f) break;
-  }
+  power_iterate(c, v, w, &s_norm, &s_delta);
   // sign = sgn(qsum . v) (ties -> +1)
   if (tid < 32) {
     double dot = 0.0;

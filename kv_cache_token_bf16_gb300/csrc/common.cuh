@@ -14,6 +14,7 @@ enum DeviceError : int {
   kDevOk = 0,
   kDevWaitTimeout = 1,   // a bounded inter-CTA wait gave up
   kDevBadIndex = 2,      // an index failed a bounds check
+  kDevNonFinite = 3,     // the key-SVD fallback met a non-finite key Gram
 };
 
 // Spin limit of every inter-CTA wait (each spin sleeps ~100 ns; ~0.4 s total).

@@ -42,7 +42,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 const char* const kKernelNames[kKidCount] = {
     "score", "score_append", "select", "compact", "calib_gram", "calib_eig",
     "curdkv_lse", "curdkv_lse_merge", "curdkv_colsum", "curdkv_colsum_merge", "curdkv_gram", "curdkv_eig", "curdkv_leverage",
-    "evict1",
+    "evict1", "qfilters_freeze",
 };
 
 cudaEvent_t take_event(evict_handle* h) {
@@ -97,7 +97,7 @@ size_t arena_layout(evict_handle* h, char* base) {
   h->vst = cv.take<void>(bh * h->cap * kHeadDim * e);
   h->pos_st = cv.take<int32_t>(bh * h->cap * 4);
   h->score_st = cv.take<float>(bh * h->cap * 4);
-  h->filters = cv.take<float>((size_t)c.n_kv_heads * kHeadDim * 4);
+  h->filters = cv.take<float>((h->fallback ? bh : (size_t)c.n_kv_heads) * kHeadDim * 4);
   h->new_score = cv.take<float>(bh * c.max_block * 4);
   h->src_map = cv.take<int32_t>(bh * h->cap * 4);
   h->meta = cv.take<int2>(bh * sizeof(int2));
@@ -110,6 +110,9 @@ size_t arena_layout(evict_handle* h, char* base) {
   if (c.method == EVICT_CURDKV) curdkv_layout(h, &cv.off, base);
   return align_up(cv.off, 256);
 }
+
+// Keys the Q-Filters key-SVD fallback observes before it freezes its filters.
+int fallback_tokens(const evict_config* c) { return c->calib_tokens > 0 ? c->calib_tokens : 128; }
 
 int validate(const evict_config* c) {
   if (!c) return fail(EVICT_EINVAL, "config is NULL");
@@ -127,15 +130,16 @@ int validate(const evict_config* c) {
   if (c->max_kept < 0) return fail(EVICT_EINVAL, "max_kept must be >= 0");
   if (c->method == EVICT_QFILTERS) {
     if (c->sign != 1 && c->sign != -1) return fail(EVICT_EINVAL, "sign must be +1 or -1 (got %d)", c->sign);
-    if (!c->filters) return fail(EVICT_EINVAL, "Q-Filters needs calibrated filters (filters is NULL)");
-    if (c->n_filter_heads != 0 && c->n_filter_heads != c->n_kv_heads)
+    if (c->calib_tokens < 0) return fail(EVICT_EINVAL, "calib_tokens must be >= 0 (0 = default 128)");
+    if (c->filters && c->n_filter_heads != 0 && c->n_filter_heads != c->n_kv_heads)
       return fail(EVICT_EINVAL, "filters hold %d heads but the layer has %d KV heads", c->n_filter_heads, c->n_kv_heads);
   }
   if (c->method == EVICT_KNORM && c->keep_low != 0 && c->keep_low != 1)
     return fail(EVICT_EINVAL, "keep_low must be 0 or 1");
   if (c->method == EVICT_CURDKV && (c->rank_cap < 0 || c->rank_cap > kCurdkvMaxRank))
     return fail(EVICT_ELIMIT, "rank_cap must be in [1, %d] (0 = default 16)", kCurdkvMaxRank);
-  const long long cap = std::max(c->budget, c->max_kept);
+  long long cap = std::max(c->budget, c->max_kept);
+  if (c->method == EVICT_QFILTERS && !c->filters) cap = std::max(cap, (long long)fallback_tokens(c) - 1);
   if (cap + c->max_block > EVICT_MAX_SELECT_ROWS)
     return fail(EVICT_ELIMIT, "capacity %lld + max_block %d exceeds %d rows per (b,h)", cap, c->max_block,
                 EVICT_MAX_SELECT_ROWS);
@@ -166,6 +170,8 @@ GroupParams make_group_params(const evict_handle* h, int m, int n_layers) {
   P.s.n_layers = n_layers;
   P.s.keep_low = c.method == EVICT_KNORM ? c.keep_low : 0;
   P.s.sign = (float)(c.method == EVICT_QFILTERS ? c.sign : 1);
+  P.s.filter_per_unit = h->fallback ? 1 : 0;
+  P.s.zero_scores = h->fallback && !h->frozen ? 1 : 0;
   P.s.method = c.method;
   P.s.offset = h->offset;
   P.err = h->err;
@@ -209,6 +215,7 @@ bool same_shape(const evict_handle* a, const evict_handle* b) {
   return x.method == y.method && x.dtype == y.dtype && x.batch == y.batch && x.n_kv_heads == y.n_kv_heads &&
          x.budget == y.budget && x.n_sink == y.n_sink && x.recent == y.recent && x.keep_low == y.keep_low &&
          x.sign == y.sign && x.rank_cap == y.rank_cap && a->cap == b->cap && a->new_stride == b->new_stride &&
+         a->fallback == b->fallback && a->frozen == b->frozen && x.calib_tokens == y.calib_tokens &&
          a->n_kept == b->n_kept && a->offset == b->offset && a->stream == b->stream;
 }
 
@@ -220,6 +227,23 @@ int run_intrinsic(evict_handle* const* hs, int n_layers, const void* const* k, c
   for (int l = 0; l < n_layers; ++l) P.L[l] = make_layer_ptrs(hs[l], k[l], v[l], pos ? pos[l] : nullptr);
   const long long n = (long long)h->n_kept + m;
   cudaError_t e;
+  if (h->fallback && !h->frozen) {
+    if (h->offset + m < h->cfg.calib_tokens) {
+      // no filter yet: keep every row (n <= offset + m < calib_tokens <= cap + 1)
+      e = timed_launch(h, kKidAppend, [&] { return launch_append(P, h->elem, h->stream); });
+      if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
+      for (int l = 0; l < n_layers; ++l) {
+        hs[l]->n_kept = (int)n;
+        hs[l]->last_evicted = false;
+        hs[l]->offset += m;
+      }
+      return EVICT_OK;
+    }
+    e = timed_launch(h, kKidFreeze, [&] { return launch_freeze(P, h->elem, h->stream); });
+    if (e != cudaSuccess) return cuda_fail(e, "fallback freeze kernel launch");
+    for (int l = 0; l < n_layers; ++l) hs[l]->frozen = true;
+    P.s.zero_scores = 0;
+  }
   if (n <= h->cfg.budget) {
     e = timed_launch(h, kKidAppend, [&] { return launch_append(P, h->elem, h->stream); });
     if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
@@ -277,8 +301,11 @@ int evict_init(const evict_config* cfg, evict_handle** out) {
   h->cfg = *cfg;
   if (h->cfg.method == EVICT_CURDKV && h->cfg.rank_cap == 0) h->cfg.rank_cap = 16;
   h->cfg.filters = nullptr;
+  h->fallback = cfg->method == EVICT_QFILTERS && !cfg->filters;
+  h->cfg.calib_tokens = h->fallback ? fallback_tokens(cfg) : 0;
   h->elem = cfg->dtype == EVICT_BF16 ? 2 : 4;
   h->cap = std::max(cfg->budget, cfg->max_kept);
+  if (h->fallback) h->cap = std::max(h->cap, h->cfg.calib_tokens - 1);
   h->new_stride = cfg->max_block;
   h->chunk = compact_chunk_rows(h->elem);
   h->flag_stride = compact_flag_slots(h->cap, h->elem);
@@ -299,7 +326,8 @@ int evict_init(const evict_config* cfg, evict_handle** out) {
   if ((e = cudaMemsetAsync(h->arena, 0, bytes, h->stream)) != cudaSuccess) return bail(e, "clearing the cache");
   if ((e = prepare_select()) != cudaSuccess) return bail(e, "select kernel attribute");
   if ((e = prepare_evict1()) != cudaSuccess) return bail(e, "single-eviction kernel attribute");
-  if (cfg->method == EVICT_QFILTERS) {
+  if (h->fallback && (e = prepare_freeze()) != cudaSuccess) return bail(e, "freeze kernel attribute");
+  if (cfg->method == EVICT_QFILTERS && !h->fallback) {
     const size_t fb = (size_t)cfg->n_kv_heads * kHeadDim * sizeof(float);
     if ((e = cudaMemcpyAsync(h->filters, cfg->filters, fb, cudaMemcpyDeviceToDevice, h->stream)) != cudaSuccess)
       return bail(e, "copying the filters");
@@ -400,7 +428,8 @@ int evict_stats(const evict_handle* h, evict_stats_t* out) {
   out->tokens_seen = h->offset;
   out->tokens_kept = h->n_kept;
   out->kept_bytes = per_token * h->n_kept;
-  if (c.method == EVICT_QFILTERS) out->kept_bytes += (int64_t)c.n_kv_heads * kHeadDim * 4;
+  if (c.method == EVICT_QFILTERS && !h->fallback) out->kept_bytes += (int64_t)c.n_kv_heads * kHeadDim * 4;
+  if (h->fallback && h->frozen) out->kept_bytes += (int64_t)c.batch * c.n_kv_heads * kHeadDim * 4;
   out->full_seq_bytes = per_token * h->offset;
   out->compression_ratio = out->kept_bytes ? (double)out->full_seq_bytes / (double)out->kept_bytes : 0.0;
   out->offset = h->offset;
@@ -443,6 +472,7 @@ int evict_reset(evict_handle* h) {
   h->n_kept = 0;
   h->offset = 0;
   h->last_evicted = false;
+  h->frozen = false;          // the fallback estimates new filters for the next sequence
   return EVICT_OK;
 }
 
@@ -463,7 +493,9 @@ int evict_sync(evict_handle* h) {
   if (err) {
     cudaMemset(h->err, 0, sizeof(int));
     return fail(EVICT_EDEVICE, "a kernel reported device error %d (%s)", err,
-                err == kDevWaitTimeout ? "bounded wait timed out" : "index check failed");
+                err == kDevWaitTimeout  ? "bounded wait timed out"
+                : err == kDevNonFinite ? "non-finite key Gram at the fallback freeze"
+                                       : "index check failed");
   }
   return EVICT_OK;
 }
@@ -527,6 +559,20 @@ int evict_compaction_rows(evict_handle* h, int64_t* old_moved, int64_t* new_writ
     *old_moved += m.y - m.x;
     *new_written += h->cfg.budget - m.y;
   }
+  return EVICT_OK;
+}
+
+int evict_qfilters_filters(evict_handle* h, float* out_host, int* n_rows) {
+  if (!h || !n_rows) return fail(EVICT_EINVAL, "handle and n_rows must not be NULL");
+  if (h->cfg.method != EVICT_QFILTERS) return fail(EVICT_EINVAL, "not a Q-Filters cache");
+  const evict_config& c = h->cfg;
+  const int rows = h->fallback ? (h->frozen ? c.batch * c.n_kv_heads : 0) : c.n_kv_heads;
+  *n_rows = rows;
+  if (!out_host || rows == 0) return EVICT_OK;
+  cudaError_t e = cudaMemcpyAsync(out_host, h->filters, (size_t)rows * kHeadDim * sizeof(float),
+                                  cudaMemcpyDeviceToHost, h->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the filters");
   return EVICT_OK;
 }
 

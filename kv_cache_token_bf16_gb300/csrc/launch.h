@@ -26,5 +26,9 @@ int evict1_max_block();
 // Raise the single-eviction kernel's dynamic shared memory limit (current device).
 cudaError_t prepare_evict1();
 cudaError_t launch_evict1(const GroupParams& P, int dtype_bytes, cudaStream_t st);
+// Q-Filters key-SVD fallback: estimate and freeze every unit's filter from the
+// keys present (kept rows, then the block) and re-score the kept rows.
+cudaError_t prepare_freeze();
+cudaError_t launch_freeze(const GroupParams& P, int dtype_bytes, cudaStream_t st);
 
 }  // namespace evict

@@ -140,7 +140,7 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
   L.vst = v_out;
   L.pos_st = pos_out;
   L.score_st = score_out;
-  L.filters = c.filters;
+  L.filters = const_cast<float*>(c.filters);   // read only: no fallback freeze here
   L.new_score = reinterpret_cast<float*>(s);
   L.src_map = reinterpret_cast<int32_t*>(s + off_src);
   L.meta = reinterpret_cast<int2*>(s + off_meta);

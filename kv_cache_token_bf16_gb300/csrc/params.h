@@ -20,7 +20,8 @@ struct LayerPtrs {
   void* vst;               // [B, H, cap, D] kept values
   int32_t* pos_st;         // [B, H, cap]
   float* score_st;         // [B, H, cap]
-  const float* filters;    // [H, D] (Q-Filters)
+  float* filters;          // Q-Filters: [H, D] calibrated, or [B, H, D] frozen by the key-SVD
+                           // fallback (written only by the freeze kernel)
   float* new_score;        // [B, H, new_stride] scores of incoming rows
   int32_t* src_map;        // [B, H, cap] source row of each kept destination
   int2* meta;              // [B, H] {first moved destination, old survivors}
@@ -44,6 +45,8 @@ struct Shape {
   int n_layers;
   int keep_low;            // KNorm keep-low: priority = -score
   float sign;              // Q-Filters sign
+  int filter_per_unit;     // Q-Filters: filters are [B, H, D] (key-SVD fallback), else [H, D]
+  int zero_scores;         // append stores score 0 (key-SVD fallback before its freeze)
   int method;
   long long offset;        // absolute position of the first incoming token
 };

@@ -250,3 +250,22 @@ def clustered_keys(seed: int, batch: int, n_kv_heads: int, length: int, spread: 
     c = unit_vectors(g, batch * n_kv_heads).reshape(batch, n_kv_heads, 1, HEAD_DIM)
     k = c + spread * g.standard_normal((batch, n_kv_heads, length, HEAD_DIM))
     return f32_to_bf16_bits(k.astype(np.float32))
+
+
+def dominant_axis_block(seed: int, batch: int, n_kv_heads: int, length: int, spread: float = 12.0,
+                        dtype: str = "bf16"):
+    """Keys with one planted dominant variance axis per (b, h), values N(0, 1).
+
+    k = N(0, I) + spread * N(0, 1) * u_bh for a seeded unit axis u_bh, so the
+    centred keys' top singular direction is u_bh up to sampling noise.
+    Returns (K, V) in the storage format ("bf16" bits or "fp32") and the axes
+    u [B, H, 128] (float64).
+    """
+    g = rng(seed)
+    u = unit_vectors(g, batch * n_kv_heads).reshape(batch, n_kv_heads, 1, HEAD_DIM)
+    t = g.standard_normal((batch, n_kv_heads, length, 1))
+    k = (g.standard_normal((batch, n_kv_heads, length, HEAD_DIM)) + spread * t * u).astype(np.float32)
+    v = g.standard_normal((batch, n_kv_heads, length, HEAD_DIM)).astype(np.float32)
+    if dtype == "bf16":
+        k, v = f32_to_bf16_bits(k), f32_to_bf16_bits(v)
+    return k, v, u[:, :, 0]

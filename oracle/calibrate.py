@@ -69,10 +69,19 @@ def key_svd_filter(keys: np.ndarray) -> np.ndarray:
     """Key-SVD fallback filter of one (b, h): keys [n, D] -> unit direction (fp64).
 
     Top right singular vector of the mean-centred keys; the largest-magnitude
-    component is made positive (the first one on ties).
+    component is made positive (the first one on ties). Two cases the page
+    leaves open: keys that are all equal have no direction, and the filter is
+    then the first coordinate axis e_0; a non-finite key has no SVD, and the
+    freeze raises ValueError.
     """
     x = to_f64(keys)
+    if not np.all(np.isfinite(x)):
+        raise ValueError("non-finite key at the key-SVD freeze")
     x = x - x.mean(axis=0, keepdims=True)
+    if not np.any(x):
+        e0 = np.zeros(x.shape[1])
+        e0[0] = 1.0
+        return e0
     _, _, vt = np.linalg.svd(x, full_matrices=False)
     v = vt[0]
     j = int(np.argmax(np.abs(v)))

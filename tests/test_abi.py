@@ -49,7 +49,9 @@ def _cfg(**kw):
     (dict(dtype=3), binding.EVICT_EINVAL),
     (dict(keep_low=2), binding.EVICT_EINVAL),
     (dict(method=binding.EVICT_QFILTERS, sign=0, filters=8), binding.EVICT_EINVAL),   # invalid sign
-    (dict(method=binding.EVICT_QFILTERS, sign=1, filters=None), binding.EVICT_EINVAL),  # no filters
+    # no filters: the key-SVD fallback, which needs calib_tokens >= 0 and keeps calib_tokens - 1 rows
+    (dict(method=binding.EVICT_QFILTERS, sign=1, filters=None, calib_tokens=-1), binding.EVICT_EINVAL),
+    (dict(method=binding.EVICT_QFILTERS, sign=1, filters=None, calib_tokens=49100), binding.EVICT_ELIMIT),
     (dict(method=binding.EVICT_QFILTERS, n_kv_heads=8, filters=8, n_filter_heads=4), binding.EVICT_EINVAL),
     (dict(method=binding.EVICT_CURDKV, dtype=binding.EVICT_FP32), binding.EVICT_EINVAL),
     (dict(method=binding.EVICT_CURDKV, rank_cap=500), binding.EVICT_ELIMIT),

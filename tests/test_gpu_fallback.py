@@ -1,0 +1,179 @@
+"""GPU parity of the Q-Filters key-SVD fallback against the CPU oracle.
+
+"Q-Filters — Query-Agnostic Projection Eviction", §How it works step 2
+(before calib_tokens keys nothing is evicted; then the filter is estimated
+from the key SVD and frozen), §Key-SVD fallback, §Path dependence.
+
+The freeze estimates a direction by an iteration on each side (power
+iteration in fp32 on the GPU, LAPACK's SVD in fp64 in the oracle), so the two
+filters agree to rounding, not bit for bit. Parity is therefore checked in
+two parts: (1) the GPU filter against the oracle's estimate on the same keys
+(signed cosine, planted-axis inputs with a wide eigengap); (2) everything
+downstream — pass-through rows, the freeze step's eviction, every later
+update — bit for bit against an oracle that freezes the GPU's filter at the
+same call.
+"""
+import numpy as np
+import pytest
+
+from kv_cache_token_bf16_gb300 import synth
+from oracle import calibrate as ocal
+from oracle.cache import OracleCache
+from tests.gpu_util import assert_cache_equal, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _pair(B, H, budget, calib, dtype="bf16", max_block=512, **kw):
+    from kv_cache_token_bf16_gb300 import binding
+    gpu = binding.EvictCache("qfilters", B, H, budget=budget, max_block=max_block, dtype=dtype, filters=None,
+                             calib_tokens=calib, **kw)
+    ref = OracleCache("qfilters", B, H, budget=budget, dtype=dtype, filters=None, calib_tokens=calib, **kw)
+    return gpu, ref
+
+
+def _step(gpu, ref, k, v, a, b):
+    """One update on both sides; the oracle freezes the GPU's filter when the GPU froze."""
+    view = gpu.update_and_fetch(to_dev(k[:, :, a:b], torch), to_dev(v[:, :, a:b], torch))
+    gpu.sync()
+    froze = ref.filters_bh is None and gpu.filters() is not None
+    if froze:
+        gf = gpu.filters()
+        ref.filter_override = lambda bb, hh: gf[bb, hh]
+    ref.update_and_fetch(k[:, :, a:b], v[:, :, a:b])
+    return view, froze
+
+
+def _feed(gpu, ref, k, v, cuts, what):
+    frozen_at = None
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        view, froze = _step(gpu, ref, k, v, a, b)
+        if froze:
+            frozen_at = b
+        assert_cache_equal(view, ref, f"{what} after [{a},{b})")
+        assert gpu.stats() == ref.stats(), f"{what}: stats after [{a},{b})"
+    return frozen_at
+
+
+def _check_filters(gpu, k, n, axes=None, tol=2e-5):
+    """GPU filters vs the oracle's key-SVD estimate over the first n keys (signed cosine)."""
+    gf = gpu.filters().astype(np.float64)
+    B, H = gf.shape[:2]
+    for b in range(B):
+        for h in range(H):
+            want = ocal.key_svd_filter(k[b, h, :n])
+            assert abs(np.linalg.norm(gf[b, h]) - 1.0) < 1e-5
+            assert gf[b, h] @ want > 1.0 - tol, (b, h, gf[b, h] @ want)
+            if axes is not None:                 # the planted axis is recovered (page: cosine > 0.99)
+                assert abs(gf[b, h] @ axes[b, h]) > 0.99
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("chunk", [1, 7, 64, 300])
+def test_fallback_chunked_prefill_then_decode(dtype, chunk):
+    B, H, budget, calib, S = 2, 3, 40, 128, 300
+    k, v, axes = synth.dominant_axis_block(71, B, H, S + 40, dtype=dtype)
+    gpu, ref = _pair(B, H, budget, calib, dtype=dtype, n_sink=4, recent=3)
+    cuts = list(range(0, S, chunk)) + [S]
+    frozen_at = _feed(gpu, ref, k, v, cuts, f"{dtype} chunk {chunk}")
+    # the freeze happens at the first call whose block reaches calib_tokens
+    assert frozen_at == min(c for c in cuts if c >= calib)
+    _check_filters(gpu, k, frozen_at, axes)
+    # decode: single-row evictions against the frozen filters
+    _feed(gpu, ref, k, v, list(range(S, S + 40)), f"{dtype} decode")
+    assert gpu.stats()["kept_bytes"] == B * H * budget * 2 * 128 * (2 if dtype == "bf16" else 4) + B * H * 128 * 4
+
+
+def test_fallback_passthrough_keeps_everything_over_budget():
+    B, H, budget, calib = 1, 2, 16, 100
+    k, v, _ = synth.dominant_axis_block(72, B, H, 160)
+    gpu, ref = _pair(B, H, budget, calib, n_sink=2)
+    _feed(gpu, ref, k, v, [0, 30, 60, 99], "pass-through")
+    assert gpu.filters() is None
+    kk, _, pos, score = gpu.view()
+    assert kk.shape[2] == 99 and not torch.any(score != 0)
+    assert np.array_equal(pos.cpu().numpy()[0, 0], np.arange(99))
+    frozen_at = _feed(gpu, ref, k, v, [99, 100, 160], "freeze")          # 99 + 1 reaches 100
+    assert frozen_at == 100
+    _check_filters(gpu, k, 100)
+
+
+@pytest.mark.parametrize("sign", [1, -1])
+def test_fallback_one_block_freeze_and_sign(sign):
+    B, H, budget = 2, 2, 64
+    k, v, axes = synth.dominant_axis_block(73, B, H, 600)
+    gpu, ref = _pair(B, H, budget, 128, n_sink=4, sign=sign)
+    assert _feed(gpu, ref, k, v, [0, 512, 520, 600], "one block") == 512
+    _check_filters(gpu, k, 512, axes)
+
+
+def test_fallback_calib_tokens_one_and_reset():
+    B, H = 1, 2
+    k, v, _ = synth.dominant_axis_block(74, B, H, 200)
+    gpu, ref = _pair(B, H, 32, 1, n_sink=1)
+    # a single key has no variance: the filter is e_0
+    assert _feed(gpu, ref, k, v, [0, 1], "first token") == 1
+    f = gpu.filters()
+    assert np.all(f[..., 0] == 1.0) and not np.any(f[..., 1:])
+    _feed(gpu, ref, k, v, [1, 50, 120], "after e_0 freeze")
+    # reset unfreezes: the next sequence estimates its own filters
+    gpu.reset()
+    assert gpu.filters() is None and gpu.stats()["offset"] == 0
+    ref2 = OracleCache("qfilters", B, H, budget=32, n_sink=1, filters=None, calib_tokens=1)
+    assert _feed(gpu, ref2, k, v, [120, 180, 200], "second sequence") == 180
+    _check_filters(gpu, k[:, :, 120:], 60)
+
+
+def test_fallback_grouped_update():
+    from kv_cache_token_bf16_gb300 import binding
+    B, H, L = 1, 4, 3
+    data = [synth.dominant_axis_block(80 + l, B, H, 256) for l in range(L)]
+    kw = dict(n_sink=4, recent=0)
+    caches = [binding.EvictCache("qfilters", B, H, budget=48, max_block=256, filters=None, calib_tokens=100, **kw)
+              for _ in range(L)]
+    refs = [OracleCache("qfilters", B, H, budget=48, filters=None, calib_tokens=100, **kw) for _ in range(L)]
+    for a, b in ((0, 60), (60, 130), (130, 256)):
+        ks = [to_dev(d[0][:, :, a:b], torch) for d in data]
+        vs = [to_dev(d[1][:, :, a:b], torch) for d in data]
+        views = binding.evict_update_and_fetch_group([c.handle for c in caches], [t.data_ptr() for t in ks],
+                                                     [t.data_ptr() for t in vs], None, b - a)
+        caches[0].sync()
+        for c, ref, d, vw in zip(caches, refs, data, views):
+            if ref.filters_bh is None and c.filters() is not None:
+                gf = c.filters()
+                ref.filter_override = lambda bb, hh, gf=gf: gf[bb, hh]
+            ref.update_and_fetch(d[0][:, :, a:b], d[1][:, :, a:b])
+            assert_cache_equal(binding.view_tensors(vw, B, H, "bf16"), ref, f"grouped [{a},{b})")
+    for c, d in zip(caches, data):
+        _check_filters(c, d[0], 130)
+
+
+def test_fallback_degenerate_keys():
+    from kv_cache_token_bf16_gb300 import binding
+    B, H = 1, 1
+    row = synth.f32_to_bf16_bits(np.linspace(-2, 2, 128).astype(np.float32))
+    k = np.tile(row, (B, H, 20, 1))
+    v = synth.gaussian_block(75, B, H, 20)[1]
+    gpu, ref = _pair(B, H, 8, 10, n_sink=1)
+    _feed(gpu, ref, k, v, [0, 5, 12, 20], "equal keys")                # no variance: e_0
+    f = gpu.filters()
+    assert f[0, 0, 0] == 1.0 and not np.any(f[0, 0, 1:])
+    # a NaN key at the freeze: reported by sync, the cache stays usable
+    bad = k.copy()
+    bad[0, 0, 3, 17] = 0x7FC0
+    gpu2 = binding.EvictCache("qfilters", B, H, budget=8, max_block=64, filters=None, calib_tokens=10, n_sink=1)
+    gpu2.update_and_fetch(to_dev(bad[:, :, :12], torch), to_dev(v[:, :, :12], torch))
+    with pytest.raises(binding.EvictError) as e:
+        gpu2.sync()
+    assert e.value.code == binding.EVICT_EDEVICE
+    gpu2.update_and_fetch(to_dev(k[:, :, 12:20], torch), to_dev(v[:, :, 12:20], torch))
+    gpu2.sync()

@@ -101,3 +101,19 @@ def test_budget_offset_and_unit_filters_at_every_chunk_size(chunk):
             assert c.n_kept <= max(budget, min(c.offset, 127))
         assert c.n_kept == budget and c.offset == 300
         assert np.allclose(np.linalg.norm(c.filters_bh.astype(np.float64), axis=-1), 1.0, atol=1e-6)
+
+
+def test_degenerate_freezes():
+    same = np.tile(synth.f32_to_bf16_bits(np.linspace(-1, 1, 128).astype(np.float32)), (5, 1))
+    f = ocal.key_svd_filter(same)                       # no variance: the first coordinate axis
+    assert f[0] == 1.0 and not np.any(f[1:])
+    assert np.array_equal(ocal.key_svd_filter(same[:1]), f)   # a single key is the same case
+    bad = same.copy()
+    bad[2, 7] = 0x7FC0                                  # bf16 NaN
+    with pytest.raises(ValueError):
+        ocal.key_svd_filter(bad)
+    # two distinct keys: the direction is their difference, normalised and sign-fixed
+    two = synth.f32_to_bf16_bits(np.stack([np.eye(128)[3] * 2 - np.eye(128)[9], np.zeros(128)]).astype(np.float32))
+    d = np.zeros(128)
+    d[3], d[9] = 2.0, -1.0
+    assert np.allclose(ocal.key_svd_filter(two), d / np.linalg.norm(d), atol=1e-12)
