@@ -45,6 +45,8 @@ from kv_cache_token_bf16_gb300 import synth  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# fp32 FMA peak: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz maximum SM clock
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 METRIC = "cache tokens evicted-and-compacted/sec per layer; achieved HBM GB/s vs roofline"
 UNIT = "tokens/s"
 
@@ -214,6 +216,22 @@ class StackRun:
         return w["layers"] * w["batch"] * w["heads"] * w["seq"] * (128 * 2 + 4)
 
 
+def _scorer_kwargs(w, H, torch=None):
+    """Cache arguments of a workload's scorer (w["method"]): the library method name and
+    extra keywords. Q-Filters on the decode and long-context streams: seeded unit filters
+    (decode) or the GPU calibration on the workload's queries (long context, done by the
+    caller); qfilters_fallback: no filters, the key-SVD fallback freezing after 128 keys."""
+    meth = w["method"]
+    if meth == "qfilters_fallback":
+        return "qfilters", {"filters": None, "calib_tokens": 128, "sign": 1}
+    if meth == "qfilters":
+        f = synth.decode_filters(H)
+        return "qfilters", {"filters": torch.from_numpy(f).cuda() if torch else f, "sign": 1}
+    if meth == "curdkv":
+        return "curdkv", {"rank_cap": 16}
+    return meth, {}
+
+
 class DecodeRun:
     """Decode streaming: after a 2048-token prefill, one step = one single-token update."""
 
@@ -226,8 +244,10 @@ class DecodeRun:
         ks, vs = synth.decode_steps(0, w["steps"], B, H)
         self.ks = torch.from_numpy(ks.view(np.int16)).cuda().view(torch.bfloat16)
         self.vs = torch.from_numpy(vs.view(np.int16)).cuda().view(torch.bfloat16)
-        self.cache = binding.EvictCache(w["method"], B, H, budget=w["budget"], n_sink=w["n_sink"],
-                                        recent=w["recent"], max_block=w["prefill"], stream=stream.cuda_stream)
+        meth, extra = _scorer_kwargs(w, H, torch)
+        self.cache = binding.EvictCache(meth, B, H, budget=w["budget"], n_sink=w["n_sink"],
+                                        recent=w["recent"], max_block=w["prefill"], stream=stream.cuda_stream,
+                                        **extra)
         self.handle = self.cache.handle
         self.handles = [self.handle]
         self.cache.update_and_fetch(self.k0, self.v0)
@@ -273,17 +293,17 @@ class LongContextRun:
             k, v = synth.long_context_block(blk, B, H, w["block"])
             self.k.append(torch.from_numpy(k.view(np.int16)).cuda().view(torch.bfloat16))
             self.v.append(torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16))
-        extra = {}
+        meth, extra = _scorer_kwargs(w, H, torch)
         if w["method"] == "qfilters":
             q = synth.long_context_queries(H)
             qd = torch.from_numpy(q.view(np.int16)).cuda()
             f = torch.empty((H, 128), dtype=torch.float32, device="cuda")
             binding.evict_qfilters_calibrate(qd.data_ptr(), binding.EVICT_BF16, H, q.shape[1], 128, H,
                                              f.data_ptr(), stream.cuda_stream)
-            extra = {"filters": f, "sign": 1}
-        if w["method"] == "curdkv":
-            extra = {"rank_cap": 16}
-        self.cache = binding.EvictCache(w["method"], B, H, budget=w["budget"], n_sink=w["n_sink"],
+            extra["filters"] = f
+        # the fallback freezes once per sequence, on the first block (>= 128 keys)
+        self.freeze_rows = w["block"] if w["method"] == "qfilters_fallback" else 0
+        self.cache = binding.EvictCache(meth, B, H, budget=w["budget"], n_sink=w["n_sink"],
                                         recent=w["recent"], max_block=w["block"], stream=stream.cuda_stream, **extra)
         self.handle = self.cache.handle
         self.handles = [self.handle]
@@ -505,7 +525,12 @@ def run_ours(args):
         n_launch, tot_ms = ktimes[top]
         per_launch_ms = tot_ms / n_launch
         wk = work.get(top, {})
-        if "bytes" in wk:
+        if top == "qfilters_freeze":
+            achieved = wk["flops"] / (per_launch_ms / 1e3) / 1e12
+            roof = {"kernel": top, "bound": "alu", "achieved": round(achieved, 2), "peak": FP32_FMA_TFLOPS,
+                    "unit": "TFLOP/s", "frac": round(achieved / FP32_FMA_TFLOPS, 4),
+                    "algorithmic_flops_per_launch": wk["flops"]}
+        elif "bytes" in wk:
             achieved = wk["bytes"] / (per_launch_ms / 1e3) / 1e9
             roof = {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -568,6 +593,9 @@ def algorithmic_work(run, binding):
     evict1   : the fused single-eviction step: incoming keys, every row's
                score, and the rows behind the evicted one moved down
                (K, V, position and score read and written).
+    qfilters_freeze : the key-SVD fallback's one-time freeze: every key present
+               read once, 2*D*D fp32 flops per key for the centred Gram (bound
+               by the fp32 FMA pipes, "alu").
     """
     w = run.w
     e = 2 if w["dtype"] == "bf16" else 4
@@ -587,6 +615,10 @@ def algorithmic_work(run, binding):
     out["evict1"] = {"bytes": units * m * 128 * e + units * 4 * n + new * (4 * 128 * e + 12) + old * (4 * 128 * e + 16)}
     flag_stride = -(-w["budget"] // (32 if e == 2 else 16))
     out["select"] = {"bytes": int(units * (4 * n + 4 * w["budget"] + 4 * flag_stride + 8))}
+    if getattr(run, "freeze_rows", 0):
+        # key-SVD freeze: read the keys present once; the centred Gram is 2*D*D flops per key
+        out["qfilters_freeze"] = {"bytes": units * run.freeze_rows * 128 * e,
+                                  "flops": units * run.freeze_rows * 2 * 128 * 128}
     logits = getattr(run, "logits", None)
     if logits:
         calls = run.calls_per_step
@@ -624,8 +656,9 @@ def _oracle_sample(workload, budget_s=10.0):
         return tokens, secs, f"{done} of {w['layers']} layers (one prefill update each; calibration untimed)"
     if workload == "decode":
         k0, v0 = synth.decode_prefill(w["batch"], w["heads"], w["prefill"])
-        c = OracleCache(w["method"], w["batch"], w["heads"], budget=w["budget"], n_sink=w["n_sink"],
-                        recent=w["recent"])
+        meth, kw = _scorer_kwargs(w, w["heads"])
+        c = OracleCache(meth, w["batch"], w["heads"], budget=w["budget"], n_sink=w["n_sink"],
+                        recent=w["recent"], **kw)
         c.update_and_fetch(k0, v0)
         ks, vs = synth.decode_steps(0, 64, w["batch"], w["heads"])
         t0 = time.perf_counter()
@@ -638,11 +671,10 @@ def _oracle_sample(workload, budget_s=10.0):
         return tokens, time.perf_counter() - t0, f"{done} decode steps after the 2048-token prefill"
     if workload == "long_context":
         # one (b, h) unit followed through the stream (units are independent)
-        kw = {}
+        meth, kw = _scorer_kwargs(w, w["heads"])
         if w["method"] == "qfilters":
-            kw = {"filters": ocal.calibrate(synth.long_context_queries(w["heads"]), w["heads"])[:1]
-                  .astype(np.float32), "sign": 1}
-        c = OracleCache(w["method"], 1, 1, budget=w["budget"], n_sink=w["n_sink"], recent=w["recent"], **kw)
+            kw["filters"] = ocal.calibrate(synth.long_context_queries(w["heads"]), w["heads"])[:1].astype(np.float32)
+        c = OracleCache(meth, 1, 1, budget=w["budget"], n_sink=w["n_sink"], recent=w["recent"], **kw)
         for blk in range(w["blocks"]):
             k, v = synth.long_context_block(blk, w["batch"], w["heads"], w["block"])
             t1 = time.perf_counter()
@@ -720,14 +752,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qfilters_stack")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--method", choices=["knorm", "qfilters", "curdkv"], default=None,
-                    help="scorer for the long_context and decode workloads")
+    ap.add_argument("--method", choices=["knorm", "qfilters", "qfilters_fallback", "curdkv"], default=None,
+                    help="scorer for the long_context and decode workloads (qfilters_fallback: Q-Filters "
+                         "without calibrated filters, freezing a key-SVD filter after 128 keys)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.method:
         if args.workload not in ("long_context", "decode") or (args.workload == "decode" and args.method == "curdkv"):
-            ap.error("--method applies to long_context (any scorer) and decode (knorm, qfilters)")
+            ap.error("--method applies to long_context (any scorer) and decode (all but curdkv)")
         WORKLOADS[args.workload]["method"] = args.method
     if args.impl == "reference":
         run_reference(args)

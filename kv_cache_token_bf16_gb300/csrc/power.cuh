@@ -15,11 +15,13 @@ constexpr int kMaxPowerIters = 20000;
 
 // c: shared [128][kPowerStride]; v: shared [128], a unit start vector on
 // entry and the unit iterate on exit; w: shared [128] scratch; s_norm,
-// s_delta: shared scratch words. Every thread of the CTA calls it.
-__device__ __forceinline__ void power_iterate(const float* c, float* v, float* w, float* s_norm, float* s_delta) {
+// s_delta: shared scratch words. Every thread of the CTA calls it. Stops
+// after max_iters iterations at most.
+__device__ __forceinline__ void power_iterate(const float* c, float* v, float* w, float* s_norm, float* s_delta,
+                                              int max_iters = kMaxPowerIters) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int row = tid >> 1, half = tid & 1;
-  for (int it = 0; it < kMaxPowerIters; ++it) {
+  for (int it = 0; it < max_iters; ++it) {
     float acc = 0.f;
     const float* cr = c + row * kPowerStride + half * 64;
     const float* vv = v + half * 64;
