@@ -229,7 +229,7 @@ def _scorer_kwargs(w, H, torch=None):
         return "qfilters", {"filters": torch.from_numpy(f).cuda() if torch else f, "sign": 1}
     if meth == "curdkv":
         return "curdkv", {"rank_cap": 16}
-    return meth, {}
+    return meth, {}                     # knorm, h2o
 
 
 class DecodeRun:
@@ -387,8 +387,10 @@ class CurdkvPlantedRun:
         self.kn, self.vn = dev(p["k"][:, :, S0:]), dev(p["v"][:, :, S0:])
         self.pos0 = torch.arange(S0, dtype=torch.int32, device="cuda").expand(B, H, S0).contiguous()
         self.score0 = torch.zeros((B, H, S0), dtype=torch.float32, device="cuda")
-        self.cache = binding.EvictCache("curdkv", B, H, budget=w["budget"], n_sink=w["n_sink"], recent=w["recent"],
-                                        max_block=m, max_kept=S0, rank_cap=w["rank_cap"], stream=stream.cuda_stream)
+        self.cls = p["cls"]
+        self.cache = binding.EvictCache(w["method"], B, H, budget=w["budget"], n_sink=w["n_sink"],
+                                        recent=w["recent"], max_block=m, max_kept=S0, rank_cap=w["rank_cap"],
+                                        stream=stream.cuda_stream)
         self.handle = self.cache.handle
         self.handles = [self.handle]
         self.tokens_per_step = B * H * (S0 + m)
@@ -399,6 +401,13 @@ class CurdkvPlantedRun:
     def reload(self):
         self.binding.evict_set_state(self.handle, self.k0.data_ptr(), self.v0.data_ptr(), self.pos0.data_ptr(),
                                      self.score0.data_ptr(), self.w["existing"], self.w["existing"])
+
+    def class2_retention(self):
+        """Share of class-2 (negligible-value) tokens among the kept non-sink rows after the last step
+        (the pages' CurDKV-vs-H2O comparison)."""
+        pos = self.cache.view()[2].cpu().numpy()
+        cls = np.take_along_axis(self.cls, pos.astype(np.int64), axis=2)[:, :, self.w["n_sink"]:]
+        return round(float(np.mean(cls == 2)), 4)
 
     def step(self):
         self.binding.evict_update_and_fetch(self.handle, self.kn.data_ptr(), self.vn.data_ptr(), None,
@@ -603,6 +612,8 @@ def run_ours(args):
             line["config"]["calibration_ms_per_layer"] = round(run.calib_ms, 3)
         if graph is not None:
             line["graph"] = graph
+        if hasattr(run, "class2_retention"):
+            line["config"]["class2_retention"] = run.class2_retention()
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -661,6 +672,7 @@ def algorithmic_work(run, binding):
         for k in ("curdkv_lse", "curdkv_colsum"):
             out[k] = {"flops": 2 * 128 * logits / calls, "exps": logits / calls}
         out["curdkv_gram"] = {"flops": units * n * 2 * 128 * 128}
+        out["h2o_mass"] = {"bytes": int(units * n * 16)}       # read the sum, write it, read/write the score
         out["curdkv_leverage"] = {"bytes": int(units * n * (128 * 2 + 12))}
     return out
 
@@ -728,7 +740,7 @@ def _oracle_sample(workload, budget_s=10.0):
         t0 = time.perf_counter()
         for b in range(w["batch"]):
             for h in range(w["heads"]):
-                c = OracleCache("curdkv", 1, 1, budget=w["budget"], n_sink=w["n_sink"], rank_cap=w["rank_cap"])
+                c = OracleCache(w["method"], 1, 1, budget=w["budget"], n_sink=w["n_sink"], rank_cap=w["rank_cap"])
                 c.set_state(p["k"][b:b + 1, h:h + 1, :S0], p["v"][b:b + 1, h:h + 1, :S0],
                             np.arange(S0, dtype=np.int32)[None, None], np.zeros((1, 1, S0)), S0)
                 t1 = time.perf_counter()
@@ -788,15 +800,19 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qfilters_stack")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--method", choices=["knorm", "qfilters", "qfilters_fallback", "curdkv"], default=None,
+    ap.add_argument("--method", choices=["knorm", "qfilters", "qfilters_fallback", "curdkv", "h2o"], default=None,
                     help="scorer for the long_context and decode workloads (qfilters_fallback: Q-Filters "
-                         "without calibrated filters, freezing a key-SVD filter after 128 keys)")
+                         "without calibrated filters, freezing a key-SVD filter after 128 keys) and for "
+                         "curdkv_planted (curdkv or h2o)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.method:
-        if args.workload not in ("long_context", "decode") or (args.workload == "decode" and args.method == "curdkv"):
-            ap.error("--method applies to long_context (any scorer) and decode (all but curdkv)")
+        ok = {"long_context": {"knorm", "qfilters", "qfilters_fallback", "curdkv", "h2o"},
+              "decode": {"knorm", "qfilters", "qfilters_fallback"}, "curdkv_planted": {"curdkv", "h2o"}}
+        if args.method not in ok.get(args.workload, ()):
+            ap.error("--method: long_context takes any scorer, decode knorm / qfilters / qfilters_fallback, "
+                     "curdkv_planted curdkv / h2o")
         WORKLOADS[args.workload]["method"] = args.method
     if args.impl == "reference":
         run_reference(args)

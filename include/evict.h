@@ -47,12 +47,19 @@ typedef enum evict_status {
 typedef enum evict_method {
   EVICT_KNORM = 0,     /* "L2Norm — Intrinsic Key-Norm Eviction", §How it works */
   EVICT_QFILTERS = 1,  /* "Q-Filters — Query-Agnostic Projection Eviction", §How it works */
-  EVICT_CURDKV = 2     /* "CurDKV-adapted — Value-Aware Leverage-Score Eviction", §How it works */
+  EVICT_CURDKV = 2,    /* "CurDKV-adapted — Value-Aware Leverage-Score Eviction", §How it works */
+  EVICT_H2O = 3        /* H2O-adapted: cumulative proxy-attention mass, the softmax of CurDKV's
+                          step 1 ("CurDKV-adapted", §How it works step 1; a new token starts
+                          from exactly 0, §The honesty crux item 4). Per block: query t (the
+                          incoming key k+t) attends rows i <= k+t with scale 1/sqrt(D); row i
+                          gains the weights of the queries after it (a new row not its own
+                          query's weight); kept rows add this to their cumulative score, new
+                          rows start from it; the budget highest are kept. bf16 only. */
 } evict_method;
 
 typedef enum evict_dtype {
   EVICT_BF16 = 0,
-  EVICT_FP32 = 1       /* KNorm and Q-Filters only */
+  EVICT_FP32 = 1       /* KNorm and Q-Filters only (CurDKV and H2O store bf16) */
 } evict_dtype;
 
 /* Compiled bounds (EVICT_ELIMIT above them). */
@@ -263,11 +270,14 @@ int evict_compaction_rows(evict_handle* h, int64_t* old_moved, int64_t* new_writ
  * (nothing copied). Synchronises the stream. EVICT_EINVAL for other methods. */
 int evict_qfilters_filters(evict_handle* h, float* out_host, int* n_rows);
 
-/* CurDKV diagnostics: copy the last update's proxy-attention column sums
- * and leverage of every row of the concatenation (kept rows first, then the
- * block; before compaction) to device buffers attn, leverage [B, H, n]
- * (either may be NULL); *n_rows receives n (0 before the first update).
- * Enqueued on the handle's stream. EVICT_EINVAL for other methods. */
+/* CurDKV / H2O diagnostics: copy the last update's proxy-attention column
+ * sums and score increments (CurDKV: leverage; H2O: the mass increment,
+ * which leaves out a new row's own weight) of every row of the
+ * concatenation (kept rows first, then the block; before compaction) to
+ * device buffers attn, leverage [B, H, n] (either may be NULL); *n_rows
+ * receives n (0 before the first update). For H2O both buffers receive the
+ * mass increment. Enqueued on the handle's stream. EVICT_EINVAL for other
+ * methods. */
 int evict_curdkv_scores(evict_handle* h, float* attn, float* leverage, int* n_rows);
 
 /* Process-wide count of kernels this library has launched. */

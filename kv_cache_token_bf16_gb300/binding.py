@@ -17,11 +17,11 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libevict.so")
 
 EVICT_OK, EVICT_EINVAL, EVICT_ELIMIT, EVICT_ECUDA, EVICT_EDEVICE, EVICT_ENUM = range(6)
-EVICT_KNORM, EVICT_QFILTERS, EVICT_CURDKV = range(3)
+EVICT_KNORM, EVICT_QFILTERS, EVICT_CURDKV, EVICT_H2O = range(4)
 EVICT_BF16, EVICT_FP32 = range(2)
 HEAD_DIM = 128
 MAX_GROUP = 32
-METHODS = {"knorm": EVICT_KNORM, "qfilters": EVICT_QFILTERS, "curdkv": EVICT_CURDKV}
+METHODS = {"knorm": EVICT_KNORM, "qfilters": EVICT_QFILTERS, "curdkv": EVICT_CURDKV, "h2o": EVICT_H2O}
 DTYPES = {"bf16": EVICT_BF16, "fp32": EVICT_FP32}
 
 

@@ -29,6 +29,7 @@ enum KernelId : int {
   kKidCurdkvLeverage,
   kKidEvict1,
   kKidFreeze,
+  kKidH2oMass,
   kKidCount
 };
 

@@ -99,6 +99,7 @@ struct CurdkvParams {
   int k, m, n, cap, heads, rank;
   int units;             // B * H
   float scale2;          // log2(e) / sqrt(D)
+  int self_excluded;      // H2O: a new row's column sum leaves out its own query (t > i - k)
   float* lse;
   float2* lse_part;       // [BH, kMaxLseSplit, lse_stride] per-split (max, sum)
   int lse_stride;         // max_block rounded up to 4
@@ -527,7 +528,7 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
       if (a < nq && !dead) {
         tc::fence_after_sync();
         const int tq = kQuad * kTile * u.q + kTile * a;            // first query of the accumulator
-        const bool full = kept || kTile * (u.kt - s.C) + kTile - 1 <= tq;
+        const bool full = kept || kTile * (u.kt - s.C) + kTile - 1 + p.self_excluded <= tq;
         float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
@@ -544,7 +545,8 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
               sm[3] += ex2(fmaf(v[c + 3], p.scale2, -l4.w));
             }
           } else {
-            const int first_t = i - p.k - tq - 64 * hf;              // columns c >= first_t see key i
+            // columns c >= first_t see key i (H2O: from the query after its own)
+            const int first_t = i - p.k - tq - 64 * hf + p.self_excluded;
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c >= first_t) sm[c & 3] += ex2(fmaf(v[c], p.scale2, -lh[c]));
@@ -581,6 +583,20 @@ __global__ void __launch_bounds__(256) curdkv_colsum_merge_kernel(const __grid_c
     sum += p.colpart[((size_t)q * s.bh_count + bh) * p.rows + i];
   }
   p.attn[(size_t)bh * p.rows + i] = sum;
+}
+
+// H2O-adapted cumulative mass ("CurDKV-adapted", §How it works step 1: the
+// proxy softmax H2O uses; §The honesty crux item 4: a new token starts from
+// 0): kept rows add their column sum to the stored score, new rows start
+// from theirs (their own query already left out by the column-sum pass).
+// grid = (ceil(n / 256), B*H).
+__global__ void __launch_bounds__(256) h2o_mass_kernel(const __grid_constant__ CurdkvParams p) {
+  const int bh = blockIdx.y, i = blockIdx.x * 256 + threadIdx.x;
+  if (i >= p.n) return;
+  const float a = p.attn[(size_t)bh * p.rows + i];
+  p.lev[(size_t)bh * p.rows + i] = a;
+  if (i < p.k) p.score_st[(size_t)bh * p.cap + i] += a;
+  else p.new_score[(size_t)bh * p.new_stride + (i - p.k)] = a;
 }
 
 // ---------------------------------------------------------------------------
@@ -1759,6 +1775,7 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   p.units = bh;
   p.rank = std::min(std::min(c.rank_cap, n), kHeadDim);
   p.scale2 = kLog2e / sqrtf((float)kHeadDim);
+  p.self_excluded = c.method == EVICT_H2O ? 1 : 0;
   p.lse = st.lse;
   p.lse_part = st.lse_part;
   p.lse_stride = st.lse_stride;
@@ -1812,33 +1829,41 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
     });
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV column-sum merge launch");
   }
-  e = timed_launch(h, kKidCurdkvGram, [&] {
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(p.gram_cluster * bh);
-    lc.blockDim = dim3(kGramThreads);
-    lc.dynamicSmemBytes = kGramSmem;
-    lc.stream = sm;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.gram_cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, curdkv_gram_kernel, p);
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "CurDKV Gram launch");
-  e = timed_launch(h, kKidCurdkvEig, [&] {
-    curdkv_eig_kernel<<<bh, kEigThreads, sizeof(EigSmem), sm>>>(p);
-    return cudaGetLastError();
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "CurDKV eigensolver launch");
-  e = timed_launch(h, kKidCurdkvLeverage, [&] {
-    const long long items = (long long)bh * ((p.k + kTile - 1) / kTile + (m + kTile - 1) / kTile);
-    curdkv_leverage_kernel<<<(int)std::min<long long>(st.sm_count, items), kLevThreads, kLevSmem, sm>>>(p);
-    return cudaGetLastError();
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "CurDKV leverage launch");
+  if (p.self_excluded) {
+    e = timed_launch(h, kKidH2oMass, [&] {
+      h2o_mass_kernel<<<dim3((n + 255) / 256, bh), 256, 0, sm>>>(p);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "H2O mass launch");
+  } else {
+    e = timed_launch(h, kKidCurdkvGram, [&] {
+      cudaLaunchConfig_t lc = {};
+      lc.gridDim = dim3(p.gram_cluster * bh);
+      lc.blockDim = dim3(kGramThreads);
+      lc.dynamicSmemBytes = kGramSmem;
+      lc.stream = sm;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)p.gram_cluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      lc.attrs = attr;
+      lc.numAttrs = 1;
+      return cudaLaunchKernelEx(&lc, curdkv_gram_kernel, p);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "CurDKV Gram launch");
+    e = timed_launch(h, kKidCurdkvEig, [&] {
+      curdkv_eig_kernel<<<bh, kEigThreads, sizeof(EigSmem), sm>>>(p);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "CurDKV eigensolver launch");
+    e = timed_launch(h, kKidCurdkvLeverage, [&] {
+      const long long items = (long long)bh * ((p.k + kTile - 1) / kTile + (m + kTile - 1) / kTile);
+      curdkv_leverage_kernel<<<(int)std::min<long long>(st.sm_count, items), kLevThreads, kLevSmem, sm>>>(p);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "CurDKV leverage launch");
+  }
   if (n <= c.budget) {
     e = timed_launch(h, kKidAppend, [&] {
       curdkv_append_kernel<<<dim3((m + 63) / 64, bh), 256, 0, sm>>>(p);

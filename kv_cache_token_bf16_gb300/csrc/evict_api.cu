@@ -42,7 +42,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 const char* const kKernelNames[kKidCount] = {
     "score", "score_append", "select", "compact", "calib_gram", "calib_eig",
     "curdkv_lse", "curdkv_lse_merge", "curdkv_colsum", "curdkv_colsum_merge", "curdkv_gram", "curdkv_eig", "curdkv_leverage",
-    "evict1", "qfilters_freeze",
+    "evict1", "qfilters_freeze", "h2o_mass",
 };
 
 cudaEvent_t take_event(evict_handle* h) {
@@ -74,6 +74,9 @@ void fold_events(evict_handle* h) {
 namespace {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// CurDKV and H2O share the proxy-attention pipeline and its buffers (curdkv.cu).
+bool attention_family(int method) { return method == EVICT_CURDKV || method == EVICT_H2O; }
 
 struct Carver {
   char* base;
@@ -107,7 +110,7 @@ size_t arena_layout(evict_handle* h, char* base) {
   h->k_stage = cv.take<void>(bh * c.max_block * kHeadDim * e);
   h->v_stage = cv.take<void>(bh * c.max_block * kHeadDim * e);
   h->pos_stage = cv.take<int32_t>((size_t)c.batch * c.max_block * 4);
-  if (c.method == EVICT_CURDKV) curdkv_layout(h, &cv.off, base);
+  if (attention_family(c.method)) curdkv_layout(h, &cv.off, base);
   return align_up(cv.off, 256);
 }
 
@@ -116,10 +119,10 @@ int fallback_tokens(const evict_config* c) { return c->calib_tokens > 0 ? c->cal
 
 int validate(const evict_config* c) {
   if (!c) return fail(EVICT_EINVAL, "config is NULL");
-  if (c->method < EVICT_KNORM || c->method > EVICT_CURDKV) return fail(EVICT_EINVAL, "unknown method %d", c->method);
+  if (c->method < EVICT_KNORM || c->method > EVICT_H2O) return fail(EVICT_EINVAL, "unknown method %d", c->method);
   if (c->dtype != EVICT_BF16 && c->dtype != EVICT_FP32) return fail(EVICT_EINVAL, "unknown dtype %d", c->dtype);
-  if (c->method == EVICT_CURDKV && c->dtype != EVICT_BF16)
-    return fail(EVICT_EINVAL, "CurDKV stores bf16 keys and values only");
+  if (attention_family(c->method) && c->dtype != EVICT_BF16)
+    return fail(EVICT_EINVAL, "CurDKV and H2O store bf16 keys and values only");
   if (c->batch < 1 || c->n_kv_heads < 1) return fail(EVICT_EINVAL, "batch and n_kv_heads must be >= 1");
   if (c->head_dim != EVICT_HEAD_DIM) return fail(EVICT_EINVAL, "head_dim must be %d (got %d)", EVICT_HEAD_DIM, c->head_dim);
   if (c->budget < 1) return fail(EVICT_EINVAL, "budget must be >= 1");
@@ -343,7 +346,7 @@ int evict_init(const evict_config* cfg, evict_handle** out) {
       }
     }
   }
-  if (cfg->method == EVICT_CURDKV) {
+  if (attention_family(cfg->method)) {
     rc = curdkv_prepare(h);
     if (rc) {
       cudaFree(h->arena);
@@ -361,7 +364,7 @@ int evict_update_and_fetch(evict_handle* h, const void* k, const void* v, const 
   int rc = check_update_args(h, k, v, pos, m, true);
   if (rc) return rc;
   if (m > 0) {
-    if (h->cfg.method == EVICT_CURDKV) {
+    if (attention_family(h->cfg.method)) {
       rc = curdkv_update(h, k, v, pos, m);
     } else {
       rc = run_intrinsic(&h, 1, &k, &v, &pos, m);
@@ -385,7 +388,7 @@ int evict_update_and_fetch_group(evict_handle* const* hs, int n_layers, const vo
     for (int j = 0; j < l; ++j)
       if (hs[j] == hs[l]) return fail(EVICT_EINVAL, "handle %d appears twice", l);
   }
-  if (hs[0]->cfg.method == EVICT_CURDKV) return fail(EVICT_EINVAL, "grouped update supports KNorm and Q-Filters");
+  if (attention_family(hs[0]->cfg.method)) return fail(EVICT_EINVAL, "grouped update supports KNorm and Q-Filters");
   if (m > 0) {
     int rc = run_intrinsic(hs, n_layers, k, v, pos, m);
     if (rc) return rc;
@@ -578,7 +581,7 @@ int evict_qfilters_filters(evict_handle* h, float* out_host, int* n_rows) {
 
 int evict_curdkv_scores(evict_handle* h, float* attn, float* leverage, int* n_rows) {
   if (!h || !n_rows) return fail(EVICT_EINVAL, "handle and n_rows must not be NULL");
-  if (h->cfg.method != EVICT_CURDKV) return fail(EVICT_EINVAL, "not a CurDKV cache");
+  if (!attention_family(h->cfg.method)) return fail(EVICT_EINVAL, "not a CurDKV or H2O cache");
   return curdkv_last_scores(h, attn, leverage, n_rows);
 }
 

@@ -9,7 +9,8 @@ no coordinator" on all three pages). Per call (block of m tokens):
    §How it works); assign absolute positions offset + [0, m) unless given.
 2. Score: KNorm norm / Q-Filters projection of the incoming keys, once;
    CurDKV proxy attention + leverage over the whole concatenation,
-   accumulated into the kept rows' cumulative score.
+   accumulated into the kept rows' cumulative score; H2O the proxy
+   attention mass (new rows seeded with 0, ``h2o.py``), accumulated alike.
 3. If the concatenation exceeds the budget, keep the protected top-k
    (``select.kept_indices``); otherwise keep everything.
 4. Compact in temporal order: K/V bits, positions (never renumbered —
@@ -43,18 +44,19 @@ import numpy as np
 
 from . import calibrate as _calibrate
 from . import curdkv as _curdkv
+from . import h2o as _h2o
 from . import scores as _scores
 from .bf16 import to_f64
 from .select import gather_rows, kept_indices, priority
 
-KNORM, QFILTERS, CURDKV = "knorm", "qfilters", "curdkv"
+KNORM, QFILTERS, CURDKV, H2O = "knorm", "qfilters", "curdkv", "h2o"
 
 
 class OracleCache:
     def __init__(self, method, batch, n_kv_heads, budget, n_sink=4, recent=0, keep_low=True,
                  sign=1, filters=None, rank_cap=16, head_dim=128, dtype="bf16", score_mode="canonical",
                  calib_tokens=128, filter_override=None):
-        if method not in (KNORM, QFILTERS, CURDKV):
+        if method not in (KNORM, QFILTERS, CURDKV, H2O):
             raise ValueError(f"unknown method {method}")
         if n_sink < 0 or recent < 0 or budget <= 0:
             raise ValueError("budget must be positive, n_sink and recent non-negative")
@@ -79,7 +81,7 @@ class OracleCache:
         self.k = np.zeros((batch, n_kv_heads, 0, head_dim), sdt)
         self.v = np.zeros((batch, n_kv_heads, 0, head_dim), sdt)
         self.pos = np.zeros((batch, n_kv_heads, 0), np.int32)
-        sc = np.float64 if method == CURDKV else (np.float32 if score_mode == "canonical" else np.float64)
+        sc = np.float64 if method in (CURDKV, H2O) else (np.float32 if score_mode == "canonical" else np.float64)
         self.score = np.zeros((batch, n_kv_heads, 0), sc)
         self.offset = 0
         self.last_kept = None          # indices kept by the last call, [B, H, n_kept]
@@ -148,6 +150,15 @@ class OracleCache:
                     l, _, _ = _curdkv.block_scores(k_all[b, h], v_all[b, h], m, self.rank_cap)
                     self.last_leverage[b, h] = l
                     score_all[b, h] = _curdkv.cumulative(self.score[b, h], l)
+            prio = priority(score_all, keep_low=False)
+        elif self.method == H2O:
+            score_all = np.empty(k_all.shape[:3])
+            self.last_mass = np.empty(k_all.shape[:3])
+            for b in range(self.batch):
+                for h in range(self.heads):
+                    mass = _h2o.proxy_mass(k_all[b, h], m)
+                    self.last_mass[b, h] = mass
+                    score_all[b, h] = _h2o.cumulative(self.score[b, h], mass)
             prio = priority(score_all, keep_low=False)
         elif self.fallback and self.filters_bh is None:
             if self.offset + m < self.calib_tokens:
