@@ -103,6 +103,11 @@ typedef struct evict_config {
                           on the chunking). Capacity is at least calib_tokens - 1 rows.
                           A non-finite key Gram at the freeze is reported by evict_sync
                           as EVICT_EDEVICE. evict_reset unfreezes. Ignored otherwise. */
+  int per_token;       /* CurDKV and H2O: 1 absorbs an m-token update one token at a time,
+                          each an m = 1 step ("CurDKV-adapted", §How it works: steps 1-5 per
+                          token); a full cache then sheds the unprotected row of lowest
+                          score, the lower index of equals (numpy's argmin, step 5). 0 (the
+                          default) scores the block at once. EVICT_EINVAL for other methods. */
 } evict_config;
 
 /* The kept cache after a call. Pointers are library-owned device memory,

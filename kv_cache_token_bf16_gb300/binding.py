@@ -32,7 +32,7 @@ class EvictConfig(ctypes.Structure):
         ("n_sink", ctypes.c_int), ("recent", ctypes.c_int), ("max_block", ctypes.c_int),
         ("max_kept", ctypes.c_int), ("keep_low", ctypes.c_int), ("sign", ctypes.c_int),
         ("filters", ctypes.c_void_p), ("n_filter_heads", ctypes.c_int), ("rank_cap", ctypes.c_int),
-        ("stream", ctypes.c_void_p), ("calib_tokens", ctypes.c_int),
+        ("stream", ctypes.c_void_p), ("calib_tokens", ctypes.c_int), ("per_token", ctypes.c_int),
     ]
 
 
@@ -261,7 +261,8 @@ class EvictCache:
 
     def __init__(self, method: str, batch: int, n_kv_heads: int, budget: int, n_sink: int = 4, recent: int = 0,
                  max_block: int = 8192, max_kept: int = 0, keep_low: bool = True, sign: int = 1, filters=None,
-                 rank_cap: int = 16, dtype: str = "bf16", stream=None, calib_tokens: int = 128):
+                 rank_cap: int = 16, dtype: str = "bf16", stream=None, calib_tokens: int = 128,
+                 per_token: bool = False):
         import torch
         self.method, self.batch, self.heads, self.dtype = method, batch, n_kv_heads, dtype
         self._fallback = method == "qfilters" and filters is None
@@ -271,7 +272,8 @@ class EvictCache:
         cfg = EvictConfig(method=METHODS[method], dtype=DTYPES[dtype], batch=batch, n_kv_heads=n_kv_heads,
                           head_dim=HEAD_DIM, budget=budget, n_sink=n_sink, recent=recent, max_block=max_block,
                           max_kept=max_kept, keep_low=int(keep_low), sign=sign, filters=None,
-                          n_filter_heads=0, rank_cap=rank_cap, stream=stream, calib_tokens=calib_tokens)
+                          n_filter_heads=0, rank_cap=rank_cap, stream=stream, calib_tokens=calib_tokens,
+                          per_token=int(per_token))
         if filters is not None:
             f = torch.as_tensor(filters, dtype=torch.float32).cuda().contiguous()
             if f.dim() != 2 or f.shape[1] != HEAD_DIM:

@@ -67,6 +67,9 @@ struct evict_handle {
   void* k_stage = nullptr;
   void* v_stage = nullptr;
   int32_t* pos_stage = nullptr;
+  void* tok_k = nullptr;      // per-token mode: the current token of every (b, h)
+  void* tok_v = nullptr;
+  int32_t* tok_pos = nullptr;
   evict::CurdkvState* curdkv = nullptr;
 
   int n_kept = 0;             // rows per (b, h), identical for every (b, h)

@@ -845,6 +845,14 @@ __global__ void __launch_bounds__(kGramThreads, 1) curdkv_gram_kernel(const __gr
 //      eight (one reduction per block).
 // ---------------------------------------------------------------------------
 constexpr int kEigSteps = kHeadDim - 2;            // Householder steps
+// |x|^2 below which a column of the unit-trace matrix counts as already
+// reduced and its reflection is skipped: its entries (< 1e-8) lie under the
+// fp32 rounding of the matrix (1.2e-7 of its norm, which is at most 1), and
+// beta = 1 / (sigma (sigma + |x0|)) stays below 1e16, so that the 0.5 beta^2
+// of the next update stays in range. Nearly rank-deficient G (a proxy query
+// that attends almost only to itself) leave columns of rounding noise that
+// shrink step by step and would otherwise overflow beta^2 into inf and NaN.
+constexpr float kEigTinyColumn = 1e-16f;
 constexpr int kZPad = kHeadDim + 4;                // padded vector rows
 constexpr int kBtBlock = 8;                        // reflections per back-transform block
 constexpr int kBtBlocks = (kEigSteps + kBtBlock - 1) / kBtBlock;
@@ -1055,7 +1063,7 @@ __global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid
     const float x0 = wv[2 * n + j + 1];
     const float tail = ss - x0 * x0;
     float beta = 0.f, alpha = x0, delta = 0.f;
-    if (tail > 0.f) {
+    if (tail > 0.f && ss > kEigTinyColumn) {
       const float sigma = ss * rsqrtf(ss);
       alpha = x0 >= 0.f ? -sigma : sigma;
       delta = -alpha;                                   // v[j+1] = x0 - alpha
@@ -1872,6 +1880,15 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV append launch");
     h->n_kept = n;
     h->last_evicted = false;
+  } else if (c.per_token && n == c.budget + 1) {
+    // per-token step with a full cache: one row leaves, the argmin rule on ties
+    GroupParams P = make_group_params(h, m, 1);
+    P.L[0] = make_layer_ptrs(h, k, v, pos);
+    P.s.tie_low = 1;
+    e = timed_launch(h, kKidEvict1, [&] { return launch_evict1(P, 2, sm); });
+    if (e != cudaSuccess) return cuda_fail(e, "single-eviction kernel launch");
+    h->n_kept = c.budget;
+    h->last_evicted = true;
   } else {
     GroupParams P = make_group_params(h, m, 1);
     P.L[0] = make_layer_ptrs(h, k, v, pos);

@@ -110,6 +110,11 @@ size_t arena_layout(evict_handle* h, char* base) {
   h->k_stage = cv.take<void>(bh * c.max_block * kHeadDim * e);
   h->v_stage = cv.take<void>(bh * c.max_block * kHeadDim * e);
   h->pos_stage = cv.take<int32_t>((size_t)c.batch * c.max_block * 4);
+  if (c.per_token) {
+    h->tok_k = cv.take<void>(bh * kHeadDim * e);
+    h->tok_v = cv.take<void>(bh * kHeadDim * e);
+    h->tok_pos = cv.take<int32_t>((size_t)c.batch * 4);
+  }
   if (attention_family(c.method)) curdkv_layout(h, &cv.off, base);
   return align_up(cv.off, 256);
 }
@@ -139,6 +144,9 @@ int validate(const evict_config* c) {
   }
   if (c->method == EVICT_KNORM && c->keep_low != 0 && c->keep_low != 1)
     return fail(EVICT_EINVAL, "keep_low must be 0 or 1");
+  if (c->per_token != 0 && c->per_token != 1) return fail(EVICT_EINVAL, "per_token must be 0 or 1");
+  if (c->per_token && !attention_family(c->method))
+    return fail(EVICT_EINVAL, "per-token mode is for CurDKV and H2O (the other scorers are path independent)");
   if (c->method == EVICT_CURDKV && (c->rank_cap < 0 || c->rank_cap > kCurdkvMaxRank))
     return fail(EVICT_ELIMIT, "rank_cap must be in [1, %d] (0 = default 16)", kCurdkvMaxRank);
   long long cap = std::max(c->budget, c->max_kept);
@@ -278,6 +286,28 @@ int run_intrinsic(evict_handle* const* hs, int n_layers, const void* const* k, c
   return EVICT_OK;
 }
 
+// Per-token mode: the block's tokens one at a time, each gathered into the
+// handle's token buffers (one strided copy per tensor) and absorbed as an
+// m = 1 update.
+int per_token_update(evict_handle* h, const void* k, const void* v, const int32_t* pos, int m) {
+  const size_t bh = (size_t)h->cfg.batch * h->cfg.n_kv_heads;
+  const size_t row = kHeadDim * (size_t)h->elem;
+  for (int t = 0; t < m; ++t) {
+    cudaError_t e;
+    if ((e = cudaMemcpy2DAsync(h->tok_k, row, static_cast<const char*>(k) + t * row, m * row, row, bh,
+                               cudaMemcpyDeviceToDevice, h->stream)) != cudaSuccess ||
+        (e = cudaMemcpy2DAsync(h->tok_v, row, static_cast<const char*>(v) + t * row, m * row, row, bh,
+                               cudaMemcpyDeviceToDevice, h->stream)) != cudaSuccess)
+      return cuda_fail(e, "gathering a token");
+    if (pos && (e = cudaMemcpy2DAsync(h->tok_pos, sizeof(int32_t), pos + t, m * sizeof(int32_t), sizeof(int32_t),
+                                      h->cfg.batch, cudaMemcpyDeviceToDevice, h->stream)) != cudaSuccess)
+      return cuda_fail(e, "gathering a position");
+    int rc = curdkv_update(h, h->tok_k, h->tok_v, pos ? h->tok_pos : nullptr, 1);
+    if (rc) return rc;
+  }
+  return EVICT_OK;
+}
+
 // `device`: k, v (and pos) are read by the kernels directly, so they must be
 // aligned for 16-byte vector and TMA loads (4 bytes for positions).
 int check_update_args(const evict_handle* h, const void* k, const void* v, const int32_t* pos, int m, bool device) {
@@ -365,7 +395,7 @@ int evict_update_and_fetch(evict_handle* h, const void* k, const void* v, const 
   if (rc) return rc;
   if (m > 0) {
     if (attention_family(h->cfg.method)) {
-      rc = curdkv_update(h, k, v, pos, m);
+      rc = h->cfg.per_token && m > 1 ? per_token_update(h, k, v, pos, m) : curdkv_update(h, k, v, pos, m);
     } else {
       rc = run_intrinsic(&h, 1, &k, &v, &pos, m);
     }

@@ -47,6 +47,7 @@ struct Shape {
   float sign;              // Q-Filters sign
   int filter_per_unit;     // Q-Filters: filters are [B, H, D] (key-SVD fallback), else [H, D]
   int zero_scores;         // append stores score 0 (key-SVD fallback before its freeze)
+  int tie_low;             // single eviction: of equal lowest scores the lower index leaves
   int method;
   long long offset;        // absolute position of the first incoming token
 };

@@ -147,18 +147,19 @@ namespace {
 // compact in temporal order). Used when the concatenation exceeds the budget
 // by exactly one row (decode steps): the evicted row is the unprotected row
 // of lowest priority, the last one in (priority desc, index asc) order, i.e.
-// the largest index among the lowest keys. Every row after it moves down by
-// one. One CTA per (layer, b, h):
-//   1. score the m incoming rows (same canonical order as score_kernel);
-//   2. block-wide max of (~key << 32 | index) over the unprotected rows;
-//   3. write destinations [min(e, k), n - 1): destination d takes row d
-//      below e (incoming rows, read from the block) and row d + 1 from e on
-//      (in place for kept rows). Lane l of a warp owns one 16-byte column of
-//      K or V (lanes 0 / 16 also the position and score words) and walks
-//      the warp's destination span in increasing order, so each address is
-//      read before the same lane overwrites it; a warp's last source row can
-//      be the next warp's first destination, so every warp loads that row
-//      before a barrier.
+// the largest index among the lowest keys; with tie_low (the per-token
+// argmin of "CurDKV-adapted — Value-Aware Leverage-Score Eviction", §How it
+// works step 5) the smallest index among them. Every row after it moves down
+// by one. One CTA per (layer, b, h):
+//   1. score the m incoming rows (same canonical order as score_kernel); the
+//      kCurDKV variant (CurDKV and H2O per-token steps) takes the scores the
+//      attention pipeline left in new_score instead;
+//   2. block-wide max of (~key << 32 | tag) over the unprotected rows, the
+//      tag being the index (or its complement with tie_low);
+//   3. destinations [min(e, k), n - 1) take row d below e and row d + 1 from
+//      e on: the kept rows behind e stream through a shared-memory ring of
+//      bulk copies (step 3 below), positions and scores through shared
+//      memory, then the incoming rows are copied from the block.
 // grid = n_layers * B * H, block = 256.
 // ---------------------------------------------------------------------------
 constexpr int kE1Threads = 256;
@@ -201,15 +202,20 @@ __global__ void __launch_bounds__(kE1Threads, 2) evict1_kernel(const __grid_cons
 
   // the kept rows' candidates first (their loads overlap the scoring below)
   const int lo = s.n_sink, hi = n - s.recent;
-  unsigned long long best = 0ull;                       // (~key << 32 | index), largest = evicted
+  // (~key << 32 | tag), largest = evicted; the tag is the index, or its complement when equal
+  // scores evict the lower index (tie_low)
+  const uint32_t tag_mask = s.tie_low ? 0xffffffffu : 0u;
+  unsigned long long best = 0ull;
   for (int i = lo + tid; i < min(hi, s.k); i += kE1Threads) {
     const float sc = L.score_st[plane + i];
     const uint32_t key = order_key(s.keep_low ? -sc : sc);
-    const unsigned long long v = ((unsigned long long)(~key) << 32) | (uint32_t)i;
+    const unsigned long long v = ((unsigned long long)(~key) << 32) | ((uint32_t)i ^ tag_mask);
     best = v > best ? v : best;
   }
-  // 1. scores of the incoming rows (half-warp per row)
-  {
+  // 1. scores of the incoming rows (half-warp per row); given by the caller for kCurDKV
+  if constexpr (kMethod == kCurDKV) {
+    for (int t = tid; t < s.m; t += kE1Threads) s_new[t] = L.new_score[(size_t)bh * s.new_stride + t];
+  } else {
     const int c = tid & 15, hw = tid >> 4;
     float f[8];
     load_filter<kMethod>(L.filters, filter_row(s, bh), c, f);
@@ -228,7 +234,7 @@ __global__ void __launch_bounds__(kE1Threads, 2) evict1_kernel(const __grid_cons
   // 2. the evicted row: largest (~key, index) over the unprotected rows
   for (int i = max(lo, s.k) + tid; i < hi; i += kE1Threads) {
     const uint32_t key = order_key(s.keep_low ? -s_new[i - s.k] : s_new[i - s.k]);
-    const unsigned long long v = ((unsigned long long)(~key) << 32) | (uint32_t)i;
+    const unsigned long long v = ((unsigned long long)(~key) << 32) | ((uint32_t)i ^ tag_mask);
     best = v > best ? v : best;
   }
 #pragma unroll
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(kE1Threads, 2) evict1_kernel(const __grid_cons
   unsigned long long all = s_best[0];
 #pragma unroll
   for (int w = 1; w < kE1Warps; ++w) all = s_best[w] > all ? s_best[w] : all;
-  const int e = (int)(uint32_t)all;                     // lo <= e < hi
+  const int e = (int)((uint32_t)all ^ tag_mask);         // lo <= e < hi
 
   // 3. destinations [min(e, k), n - 1): d takes source d below e and d + 1
   // from e on. Kept rows behind e move down by one row in place: one thread
@@ -347,7 +353,8 @@ cudaError_t prepare_evict1() {
   if ((e = cudaFuncSetAttribute(evict1_kernel<true, kKNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize, kE1Smem)) ||
       (e = cudaFuncSetAttribute(evict1_kernel<false, kKNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize, kE1Smem)) ||
       (e = cudaFuncSetAttribute(evict1_kernel<true, kQFilters>, cudaFuncAttributeMaxDynamicSharedMemorySize, kE1Smem)) ||
-      (e = cudaFuncSetAttribute(evict1_kernel<false, kQFilters>, cudaFuncAttributeMaxDynamicSharedMemorySize, kE1Smem)))
+      (e = cudaFuncSetAttribute(evict1_kernel<false, kQFilters>, cudaFuncAttributeMaxDynamicSharedMemorySize, kE1Smem)) ||
+      (e = cudaFuncSetAttribute(evict1_kernel<true, kCurDKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kE1Smem)))
     return e;
   return cudaSuccess;
 }
@@ -357,6 +364,8 @@ cudaError_t launch_evict1(const GroupParams& P, int dtype_bytes, cudaStream_t st
   const bool bf = dtype_bytes == 2;
   if (P.s.method == kKNorm)
     return launch(bf ? evict1_kernel<true, kKNorm> : evict1_kernel<false, kKNorm>, grid, kE1Threads, kE1Smem, st, P);
+  if (P.s.method >= kCurDKV)          // CurDKV and H2O: scores already in new_score, bf16 storage
+    return launch(evict1_kernel<true, kCurDKV>, grid, kE1Threads, kE1Smem, st, P);
   return launch(bf ? evict1_kernel<true, kQFilters> : evict1_kernel<false, kQFilters>, grid, kE1Threads, kE1Smem, st,
                 P);
 }

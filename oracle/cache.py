@@ -47,7 +47,7 @@ from . import curdkv as _curdkv
 from . import h2o as _h2o
 from . import scores as _scores
 from .bf16 import to_f64
-from .select import gather_rows, kept_indices, priority
+from .select import gather_rows, kept_indices, kept_indices_argmin, priority
 
 KNORM, QFILTERS, CURDKV, H2O = "knorm", "qfilters", "curdkv", "h2o"
 
@@ -55,7 +55,7 @@ KNORM, QFILTERS, CURDKV, H2O = "knorm", "qfilters", "curdkv", "h2o"
 class OracleCache:
     def __init__(self, method, batch, n_kv_heads, budget, n_sink=4, recent=0, keep_low=True,
                  sign=1, filters=None, rank_cap=16, head_dim=128, dtype="bf16", score_mode="canonical",
-                 calib_tokens=128, filter_override=None):
+                 calib_tokens=128, filter_override=None, per_token=False):
         if method not in (KNORM, QFILTERS, CURDKV, H2O):
             raise ValueError(f"unknown method {method}")
         if n_sink < 0 or recent < 0 or budget <= 0:
@@ -73,6 +73,9 @@ class OracleCache:
             raise ValueError("calib_tokens must be >= 1")
         if method == CURDKV and rank_cap <= 0:
             raise ValueError("rank_cap must be positive")
+        if per_token and method not in (CURDKV, H2O):
+            raise ValueError("per-token mode is for CurDKV and H2O")
+        self.per_token = per_token
         self.method, self.batch, self.heads, self.d = method, batch, n_kv_heads, head_dim
         self.budget, self.n_sink, self.recent = budget, n_sink, recent
         self.keep_low, self.sign, self.filters, self.rank_cap = keep_low, sign, filters, rank_cap
@@ -130,9 +133,20 @@ class OracleCache:
         return _scores.projection_plain(k_new, self.filters, self.sign)
 
     def update_and_fetch(self, k_new, v_new, pos=None):
-        """Absorb one block [B, H, m, D]; return (K, V, pos, score) kept arrays."""
+        """Absorb one block [B, H, m, D]; return (K, V, pos, score) kept arrays.
+
+        Per-token mode (CurDKV, H2O): the block is absorbed one token at a
+        time, each an m = 1 call whose single eviction takes the argmin rule
+        ("CurDKV-adapted", §How it works: every incoming token goes through
+        steps 1-5, prefill and decode alike).
+        """
         m = k_new.shape[2]
         if m == 0:
+            return self.k, self.v, self.pos, self.score
+        if self.per_token and m > 1:
+            for t in range(m):
+                self.update_and_fetch(k_new[:, :, t:t + 1], v_new[:, :, t:t + 1],
+                                      None if pos is None else np.asarray(pos)[:, t:t + 1])
             return self.k, self.v, self.pos, self.score
         if pos is None:
             pos_new = np.broadcast_to(self.offset + np.arange(m, dtype=np.int64),
@@ -174,7 +188,9 @@ class OracleCache:
         else:
             score_all = np.concatenate([self.score, self._score_new(k_new).astype(self.score.dtype)], axis=2)
             prio = priority(score_all, keep_low=(self.method == KNORM and self.keep_low))
-        idx = kept_indices(prio, self.n_sink, self.recent, self.budget)
+        self.last_scores = score_all           # every row's score before this call's selection
+        select = kept_indices_argmin if self.per_token else kept_indices
+        idx = select(prio, self.n_sink, self.recent, self.budget)
         self.last_kept = idx
         self.k, self.v = gather_rows(k_all, idx), gather_rows(v_all, idx)
         self.pos, self.score = gather_rows(pos_all, idx), gather_rows(score_all, idx)

@@ -68,6 +68,21 @@ def kept_indices(prio: np.ndarray, n_sink: int, recent: int, budget: int) -> np.
     return np.sort(np.concatenate([prot, chosen], axis=-1), axis=-1)
 
 
+def kept_indices_argmin(prio: np.ndarray, n_sink: int, recent: int, budget: int) -> np.ndarray:
+    """Per-token eviction ("CurDKV-adapted", §How it works step 5): when the
+    rows exceed the budget by one, the unprotected row of lowest priority
+    leaves; on equal priorities the first one (numpy's argmin). Protected
+    rows count as +inf. Any other row count falls back to ``kept_indices``.
+    """
+    n = prio.shape[-1]
+    if n != budget + 1:
+        return kept_indices(prio, n_sink, recent, budget)
+    p = np.where(protected_mask(n, n_sink, recent), np.inf, prio)
+    e = np.argmin(p, axis=-1)
+    idx = np.broadcast_to(np.arange(n), prio.shape)
+    return idx[idx != e[..., None]].reshape(prio.shape[:-1] + (budget,))
+
+
 def kept_indices_bruteforce(prio: np.ndarray, n_sink: int, recent: int, budget: int) -> np.ndarray:
     """Same selection by pairwise counting on one (b, h) row (tiny n only).
 

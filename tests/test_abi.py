@@ -54,6 +54,9 @@ def _cfg(**kw):
     (dict(method=binding.EVICT_QFILTERS, sign=1, filters=None, calib_tokens=49100), binding.EVICT_ELIMIT),
     (dict(method=binding.EVICT_QFILTERS, n_kv_heads=8, filters=8, n_filter_heads=4), binding.EVICT_EINVAL),
     (dict(method=binding.EVICT_CURDKV, dtype=binding.EVICT_FP32), binding.EVICT_EINVAL),
+    (dict(method=binding.EVICT_H2O, dtype=binding.EVICT_FP32), binding.EVICT_EINVAL),
+    (dict(method=binding.EVICT_KNORM, per_token=1), binding.EVICT_EINVAL),          # per-token: CurDKV/H2O only
+    (dict(method=binding.EVICT_CURDKV, per_token=2), binding.EVICT_EINVAL),
     (dict(method=binding.EVICT_CURDKV, rank_cap=500), binding.EVICT_ELIMIT),
     (dict(budget=40000, max_block=20000), binding.EVICT_ELIMIT),  # raised, never truncated
 ])
