@@ -390,13 +390,18 @@ class CurdkvPlantedRun:
         self.cls = p["cls"]
         self.cache = binding.EvictCache(w["method"], B, H, budget=w["budget"], n_sink=w["n_sink"],
                                         recent=w["recent"], max_block=m, max_kept=S0, rank_cap=w["rank_cap"],
-                                        stream=stream.cuda_stream)
+                                        stream=stream.cuda_stream, per_token=w.get("per_token", False))
         self.handle = self.cache.handle
         self.handles = [self.handle]
         self.tokens_per_step = B * H * (S0 + m)
         self.calls_per_step = 1
         self.rows_per_call = S0 + m
         self.logits = B * H * (m * S0 + m * (m + 1) // 2)
+        if w.get("per_token"):
+            # m single-token steps: the first sees every existing row, the rest a full cache of
+            # budget + 1 rows; the per-launch work of the attention kernels varies, so the kernel
+            # table carries times only
+            self.logits = None
 
     def reload(self):
         self.binding.evict_set_state(self.handle, self.k0.data_ptr(), self.v0.data_ptr(), self.pos0.data_ptr(),
@@ -740,7 +745,8 @@ def _oracle_sample(workload, budget_s=10.0):
         t0 = time.perf_counter()
         for b in range(w["batch"]):
             for h in range(w["heads"]):
-                c = OracleCache(w["method"], 1, 1, budget=w["budget"], n_sink=w["n_sink"], rank_cap=w["rank_cap"])
+                c = OracleCache(w["method"], 1, 1, budget=w["budget"], n_sink=w["n_sink"], rank_cap=w["rank_cap"],
+                                per_token=w.get("per_token", False))
                 c.set_state(p["k"][b:b + 1, h:h + 1, :S0], p["v"][b:b + 1, h:h + 1, :S0],
                             np.arange(S0, dtype=np.int32)[None, None], np.zeros((1, 1, S0)), S0)
                 t1 = time.perf_counter()
@@ -804,6 +810,8 @@ def main():
                     help="scorer for the long_context and decode workloads (qfilters_fallback: Q-Filters "
                          "without calibrated filters, freezing a key-SVD filter after 128 keys) and for "
                          "curdkv_planted (curdkv or h2o)")
+    ap.add_argument("--per-token", action="store_true",
+                    help="curdkv_planted: absorb the incoming block one token at a time (the pages' loop)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -814,6 +822,10 @@ def main():
             ap.error("--method: long_context takes any scorer, decode knorm / qfilters / qfilters_fallback, "
                      "curdkv_planted curdkv / h2o")
         WORKLOADS[args.workload]["method"] = args.method
+    if args.per_token:
+        if args.workload != "curdkv_planted":
+            ap.error("--per-token applies to curdkv_planted")
+        WORKLOADS[args.workload]["per_token"] = True
     if args.impl == "reference":
         run_reference(args)
     else:
