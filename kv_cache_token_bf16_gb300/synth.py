@@ -269,3 +269,44 @@ def dominant_axis_block(seed: int, batch: int, n_kv_heads: int, length: int, spr
     if dtype == "bf16":
         k, v = f32_to_bf16_bits(k), f32_to_bf16_bits(v)
     return k, v, u[:, :, 0]
+
+
+# --------------------------------------------------------------------------
+# Output-perturbation harness geometries
+# --------------------------------------------------------------------------
+PERTURB_GEOMETRIES = ("knorm_paper", "qfilters_paper", "isotropic")
+
+
+def perturbation_geometry(kind: str, seed: int, batch: int, length: int, n_probe: int = 32):
+    """Keys, values and probe queries of one harness geometry; every batch row is one trial.
+
+    Per row a seeded unit axis u; probe queries q = 8 u + 0.3 N(0, I) (a query cluster).
+      knorm_paper     half the tokens low-norm and aligned with the query cluster
+                      (k = u + 0.05 N(0, I)), half high-norm and anti-aligned
+                      (k = -2.5 u + 0.15 N(0, I)), in random order;
+      qfilters_paper  a quarter of the tokens important: a large projection on the
+                      dominant axis u and aligned with the queries (k = 3 u + 0.3 N(0, I)),
+                      the rest k = 0.5 N(0, 1) u + 0.3 N(0, I);
+      isotropic       k = N(0, I), no relation to the queries.
+    Values N(0, I). Returns (K, V) bf16 bits [B, 1, length, 128], probes float32
+    [B, n_probe, 128] and the axes u float64 [B, 128].
+    """
+    if kind not in PERTURB_GEOMETRIES:
+        raise ValueError(f"unknown geometry {kind}")
+    g = rng(seed)
+    u = unit_vectors(g, batch)                                   # [B, D]
+    q = 8.0 * u[:, None, :] + 0.3 * g.standard_normal((batch, n_probe, HEAD_DIM))
+    noise = g.standard_normal((batch, length, HEAD_DIM))
+    if kind == "knorm_paper":
+        aligned = np.stack([g.permutation(length) < length // 2 for _ in range(batch)])[..., None]
+        k = np.where(aligned, u[:, None, :] + 0.05 * noise, -2.5 * u[:, None, :] + 0.15 * noise)
+    elif kind == "qfilters_paper":
+        important = np.stack([g.permutation(length) < length // 4 for _ in range(batch)])[..., None]
+        c = np.where(important, 3.0, 0.5 * g.standard_normal((batch, length, 1)))
+        k = c * u[:, None, :] + 0.3 * noise
+    else:
+        k = noise
+    v = g.standard_normal((batch, length, HEAD_DIM))
+    kb = f32_to_bf16_bits(k[:, None].astype(np.float32))
+    vb = f32_to_bf16_bits(v[:, None].astype(np.float32))
+    return kb, vb, q.astype(np.float32), u
