@@ -5,6 +5,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "params.h"
+#include "tcgen05.cuh"
 
 namespace evict {
 namespace {
@@ -19,12 +20,15 @@ namespace {
 //   (1) takes the next chunk index of its (layer, b, h) from a per-unit
 //       counter, so a lower chunk always belongs to a CTA that is already
 //       running (every wait below ends);
-//   (2) loads its sources into registers and proves the loads complete by
-//       consuming them (an XOR into shared memory) before a barrier;
+//   (2) gathers its source rows into shared memory with one bulk copy per
+//       K / V row (all in flight at once, completing on one mbarrier) and
+//       its positions / scores into registers, consumed into shared memory
+//       before a barrier;
 //   (3) publishes a read-done flag (release) and waits (acquire, bounded)
 //       for the lower chunks whose kept-row sources lie in its destinations
 //       (a range the select kernel recorded per chunk);
-//   (4) stores.
+//   (4) writes the chunk's destination rows, which are contiguous, with one
+//       bulk store for K and one for V.
 // Rows below the first eviction never move and are not touched. Incoming
 // survivors are read straight from the caller's K/V blocks, so with no kept
 // rows (k = 0) nothing can be clobbered: the chunk is the CTA's own and no
@@ -33,14 +37,22 @@ namespace {
 // ---------------------------------------------------------------------------
 constexpr int kCompactThreads = 256;
 
+// Bounded wait on the chunk's copy barrier; raises the device error on timeout.
+__device__ __forceinline__ bool compact_wait(uint64_t* bar, int* err) {
+  for (int spin = 0; spin < (1 << 22); ++spin)
+    if (tc::mbar_try_wait(bar, 0)) return true;
+  raise_device_error(err, kDevWaitTimeout);
+  return false;
+}
+
 template <int kRowBytes, int kChunk>
 __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_constant__ GroupParams P) {
-  constexpr int kVpr = kRowBytes / 16;                       // 16-byte vectors per row
-  constexpr int kPer = kChunk * kVpr / kCompactThreads;      // vectors per thread (K and V each)
-  static_assert(kChunk * kVpr % kCompactThreads == 0, "chunk must split evenly over the CTA");
+  static_assert(kChunk <= kCompactThreads, "one thread per destination row");
+  extern __shared__ __align__(128) unsigned char c_smem[];   // the chunk's K rows, then its V rows
+  __shared__ uint64_t s_bar;
   __shared__ int s_chunk, s_abort;
   __shared__ int2 s_wait;
-  __shared__ volatile uint32_t s_sink[kCompactThreads];
+  __shared__ volatile uint32_t s_sink[kChunk];
   const Shape& s = P.s;
   const int tid = threadIdx.x;
   const int bhn = s.batch * s.heads;
@@ -54,6 +66,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
   if (tid == 0) {
     s_chunk = ordered ? atomicAdd(&flags[chunks], 1) : (int)(blockIdx.x / units);   // per-unit chunk counter
     s_abort = 0;
+    tc::mbar_init(&s_bar, 1);
   }
   __syncthreads();
   const int c = s_chunk;
@@ -62,12 +75,8 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
     return;
   }
   if (tid == 0 && ordered) s_wait = L.waits[(size_t)bh * chunks + c];   // lower chunks to wait for
-  int first = 0, old_kept = 0;
-  if (ordered) {
-    const int2 meta = L.meta[bh];
-    first = meta.x;
-    old_kept = meta.y;
-  }
+  int first = 0;
+  if (ordered) first = L.meta[bh].x;
   const int d_lo = max(c * kChunk, first);
   const int d_hi = min(c * kChunk + kChunk, s.budget);
   if (d_lo >= d_hi) {
@@ -82,34 +91,16 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
   const char* vin = static_cast<const char*>(L.v_in) + (size_t)bh * s.m * kRowBytes;
   const int rows = d_hi - d_lo;
   const int n_rows = s.k + s.m;
+  const uint32_t sk = tc::smem_u32(c_smem), sv = sk + kChunk * kRowBytes;
 
-  // (2) loads into registers
-  uint4 kr[kPer], vr[kPer];
+  // (2) sources: checked, then positions / scores into registers and K / V rows by bulk copies
+  int sr = -1;
   int32_t my_pos = 0;
   float my_score = 0.f;
-  bool bad = false;
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int idx = tid + q * kCompactThreads;
-    const int r = idx / kVpr, vec = idx - r * kVpr;
-    kr[q] = vr[q] = make_uint4(0, 0, 0, 0);
-    if (r < rows) {
-      const int sr = src[d_lo + r];
-      if (sr < 0 || sr >= n_rows) {
-        bad = true;
-      } else if (sr < s.k) {
-        kr[q] = reinterpret_cast<const uint4*>(kst + (plane + sr) * kRowBytes)[vec];
-        vr[q] = reinterpret_cast<const uint4*>(vst + (plane + sr) * kRowBytes)[vec];
-      } else {
-        kr[q] = reinterpret_cast<const uint4*>(kin + (size_t)(sr - s.k) * kRowBytes)[vec];
-        vr[q] = reinterpret_cast<const uint4*>(vin + (size_t)(sr - s.k) * kRowBytes)[vec];
-      }
-    }
-  }
   if (tid < rows) {
-    const int sr = src[d_lo + tid];
+    sr = src[d_lo + tid];
     if (sr < 0 || sr >= n_rows) {
-      bad = true;
+      s_abort = 1;
     } else if (sr < s.k) {
       my_pos = L.pos_st[plane + sr];
       my_score = L.score_st[plane + sr];
@@ -119,54 +110,63 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
       my_score = L.new_score[(size_t)bh * s.new_stride + t];
     }
   }
-  uint32_t sink = (uint32_t)my_pos ^ __float_as_uint(my_score);
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) sink ^= kr[q].x ^ kr[q].y ^ kr[q].z ^ kr[q].w ^ vr[q].x ^ vr[q].y ^ vr[q].z ^ vr[q].w;
-  s_sink[tid] = sink;                                        // consumes every loaded value
-  if (bad) s_abort = 1;
+  if (tid == 0) tc::mbar_arrive_expect_tx(&s_bar, (uint32_t)(2 * rows * kRowBytes));
   __syncthreads();
+  if (s_abort) {                                             // nothing issued yet: leave at once
+    if (tid == 0) {
+      raise_device_error(P.err, kDevBadIndex);
+      if (ordered) st_release(&flags[c], 1);
+    }
+    return;
+  }
+  if (tid < rows) {
+    const char* ks = sr < s.k ? kst + (plane + sr) * kRowBytes : kin + (size_t)(sr - s.k) * kRowBytes;
+    const char* vs = sr < s.k ? vst + (plane + sr) * kRowBytes : vin + (size_t)(sr - s.k) * kRowBytes;
+    tc::bulk_load(sk + (uint32_t)(tid * kRowBytes), ks, kRowBytes, &s_bar);
+    tc::bulk_load(sv + (uint32_t)(tid * kRowBytes), vs, kRowBytes, &s_bar);
+    s_sink[tid] = (uint32_t)my_pos ^ __float_as_uint(my_score);    // consumes the register loads
+  }
+  if (tid == 0 && !compact_wait(&s_bar, P.err)) {
+    s_abort = 1;
+    compact_wait(&s_bar, P.err);                             // the copies still in flight land first
+  }
+  __syncthreads();                                           // every source read has completed
+  if (s_abort) {
+    if (tid == 0 && ordered) st_release(&flags[c], 1);
+    return;
+  }
 
   // (3) publish, then wait for the lower chunks that read our destinations
   if (tid == 0 && ordered) {
     st_release(&flags[c], 1);
-    if (!s_abort) {
-      const int2 w = s_wait;
-      for (int j = w.x; j <= w.y && j < c; ++j) {
-        int spins = 0;
-        while (ld_acquire(&flags[j]) == 0) {
-          if (++spins > kSpinLimit) {
-            raise_device_error(P.err, kDevWaitTimeout);
-            s_abort = 1;
-            break;
-          }
-          __nanosleep(64);
+    const int2 w = s_wait;
+    for (int j = w.x; j <= w.y && j < c; ++j) {
+      int spins = 0;
+      while (ld_acquire(&flags[j]) == 0) {
+        if (++spins > kSpinLimit) {
+          raise_device_error(P.err, kDevWaitTimeout);
+          s_abort = 1;
+          break;
         }
-        if (s_abort) break;
+        __nanosleep(64);
       }
-    } else {
-      raise_device_error(P.err, kDevBadIndex);
+      if (s_abort) break;
     }
-  } else if (tid == 0 && s_abort) {
-    raise_device_error(P.err, kDevBadIndex);
   }
   __syncthreads();
   if (s_abort) return;
 
-  // (4) stores
-  char* kdst = static_cast<char*>(L.kst) + (plane + d_lo) * kRowBytes;
-  char* vdst = static_cast<char*>(L.vst) + (plane + d_lo) * kRowBytes;
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int idx = tid + q * kCompactThreads;
-    if (idx / kVpr < rows) {
-      reinterpret_cast<uint4*>(kdst)[idx] = kr[q];
-      reinterpret_cast<uint4*>(vdst)[idx] = vr[q];
-    }
+  // (4) stores: the destination rows are contiguous
+  if (tid == 0) {
+    tc::bulk_store(static_cast<char*>(L.kst) + (plane + d_lo) * kRowBytes, sk, (uint32_t)(rows * kRowBytes));
+    tc::bulk_store(static_cast<char*>(L.vst) + (plane + d_lo) * kRowBytes, sv, (uint32_t)(rows * kRowBytes));
+    tc::bulk_commit();
   }
   if (tid < rows) {
     L.pos_st[plane + d_lo + tid] = my_pos;
     L.score_st[plane + d_lo + tid] = my_score;
   }
+  if (tid == 0) tc::bulk_wait_all();
 }
 
 template <typename Kernel>
@@ -188,9 +188,12 @@ cudaError_t launch_compact(GroupParams& P, int dtype_bytes, cudaStream_t st) {
   const int chunk = compact_chunk_rows(dtype_bytes);
   const int chunks = (P.s.budget + chunk - 1) / chunk;
   P.total_ctas = chunks * P.s.n_layers * P.s.batch * P.s.heads;
+  // dynamic shared memory: the chunk's K and V rows (32 KB for either element size)
   if (dtype_bytes == 2)
-    return launch(compact_kernel<kHeadDim * 2, 64>, dim3(P.total_ctas), dim3(kCompactThreads), 0, st, P);
-  return launch(compact_kernel<kHeadDim * 4, 32>, dim3(P.total_ctas), dim3(kCompactThreads), 0, st, P);
+    return launch(compact_kernel<kHeadDim * 2, 64>, dim3(P.total_ctas), dim3(kCompactThreads), 2 * 64 * kHeadDim * 2,
+                  st, P);
+  return launch(compact_kernel<kHeadDim * 4, 32>, dim3(P.total_ctas), dim3(kCompactThreads), 2 * 32 * kHeadDim * 4,
+                st, P);
 }
 
 }  // namespace evict

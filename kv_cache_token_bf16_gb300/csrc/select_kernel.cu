@@ -86,8 +86,8 @@ __device__ __forceinline__ void store_waits(const int* wlo, const int* whi, int2
   for (int c = threadIdx.x; c < chunks; c += blockDim.x) out[c] = make_int2(wlo[c], whi[c]);
 }
 
-template <int kThreads, int kPer>
-__global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant__ GroupParams P) {
+template <int kThreads, int kPer, int kMinBlocks = 1>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __grid_constant__ GroupParams P) {
   __shared__ uint32_t hist[kBins];
   __shared__ uint32_t scan[65];
   __shared__ uint32_t s_min[32], s_max[32];
@@ -412,6 +412,15 @@ cudaError_t launch_select(const GroupParams& P, cudaStream_t st) {
   const dim3 grid(P.s.n_layers * P.s.batch * P.s.heads);
   if (n <= 256 * 4) return launch(select_kernel<256, 4>, grid, dim3(256), 0, st, P);
   if (n <= 256 * 8) return launch(select_kernel<256, 8>, grid, dim3(256), 0, st, P);
+  if (n <= 512 * 16) {
+    // more (b, h) units than SMs: 512-thread CTAs, two per SM, keep every unit in one wave
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if ((int)grid.x > sms && (int)grid.x <= 2 * sms)
+      return launch(select_kernel<512, 16, 2>, grid, dim3(512), 0, st, P);
+  }
   if (n <= 1024 * 8) return launch(select_kernel<1024, 8>, grid, dim3(1024), 0, st, P);
   if (n <= 1024 * 24) return launch(select_kernel<1024, 24>, grid, dim3(1024), 0, st, P);
   return launch(select_smem_kernel<1024>, grid, dim3(1024), (size_t)n * sizeof(uint32_t), st, P);

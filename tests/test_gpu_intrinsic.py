@@ -340,3 +340,16 @@ def test_small_cache_created_after_a_large_one_does_not_break_it():
     view = _feed(gpu, ref, k, v, [0, 8192])
     assert_cache_equal(view, ref, "large after small")
     small.close()
+
+
+@pytest.mark.parametrize("method", ["knorm", "qfilters"])
+def test_more_units_than_sms_uses_two_ctas_per_sm(method):
+    # 160 (b, h) units (more than the 152 SMs) with 2048 < n <= 8192 take the 512-thread
+    # selection variant; a prefill and a second block with kept rows
+    B, H = 20, 8
+    k, v = synth.gaussian_block(61, B, H, 5000)
+    kw = dict(n_sink=4, recent=8)
+    kw.update({"keep_low": True} if method == "knorm" else {"filters": synth.decode_filters(H), "sign": -1})
+    gpu, ref = _pair(method, B, H, 700, max_block=3000, **kw)
+    view = _feed(gpu, ref, k, v, [0, 3000, 5000], check_each=True, what="160 units")
+    assert_cache_equal(view, ref, "160 units")
