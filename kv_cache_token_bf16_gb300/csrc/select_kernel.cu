@@ -68,13 +68,11 @@ constexpr int kMaxWaitChunks = (EVICT_MAX_SELECT_ROWS + 31) / 32;
 
 // Wait ranges of the compaction: a survivor with destination d and kept
 // source sr (sr < k) is read by chunk d / C and overwritten by chunk sr / C;
-// when those differ the overwriting chunk must wait for the reading one.
-__device__ __forceinline__ void note_wait(int* wlo, int* whi, int d, int sr, int chunk) {
-  const int cd = d / chunk, cs = sr / chunk;
-  if (cd < cs) {
-    atomicMin(&wlo[cs], cd);
-    atomicMax(&whi[cs], cd);
-  }
+// when those differ the overwriting chunk cs must wait for the reading chunks
+// [lo, hi].
+__device__ __forceinline__ void note_wait_range(int* wlo, int* whi, int cs, int lo, int hi) {
+  atomicMin(&wlo[cs], lo);
+  atomicMax(&whi[cs], hi);
 }
 __device__ __forceinline__ void init_waits(int* wlo, int* whi, int chunks) {
   for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
@@ -222,6 +220,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __gr
   int32_t* src_map = L.src_map + (size_t)bh * s.cap;
   int first_drop = s.k;
   uint32_t old_kept = 0u;
+  // wait ranges: the thread's rows and destinations both increase, so each source chunk's
+  // destination chunks form one run; it is recorded once per run
+  int run_cs = -1, run_lo = 0, run_hi = -1;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int i = i0 + j;
@@ -231,13 +232,22 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __gr
       else raise_device_error(P.err, kDevBadIndex);
       if (i < s.k) {
         ++old_kept;
-        note_wait(s_wlo, s_whi, (int)dest, i, s.chunk);
+        const int cd = (int)dest / s.chunk, cs = i / s.chunk;
+        if (cd < cs) {
+          if (cs != run_cs) {
+            if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
+            run_cs = cs;
+            run_lo = cd;
+          }
+          run_hi = cd;
+        }
       }
       ++dest;
     } else if (i < s.k && i < first_drop) {
       first_drop = i;
     }
   }
+  if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
   if (first_drop < s.k) atomicMin(&s_first, first_drop);
   const uint32_t wsum = __reduce_add_sync(0xffffffffu, old_kept);
   if (lane == 0 && wsum) atomicAdd(&s_old_kept, (int)wsum);
@@ -365,6 +375,7 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
   uint32_t old_kept = 0u;
   {
     uint32_t eb = eq_before;
+    int run_cs = -1, run_lo = 0, run_hi = -1;           // wait ranges, one record per run (as above)
     for (int i = i_begin; i < i_end; ++i) {
       const bool prot = i < lo || i >= hi;
       const uint32_t key = keys[i];
@@ -375,13 +386,22 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
         else raise_device_error(P.err, kDevBadIndex);
         if (i < s.k) {
           ++old_kept;
-          note_wait(s_wlo, s_whi, (int)dest, i, s.chunk);
+          const int cd = (int)dest / s.chunk, cs = i / s.chunk;
+          if (cd < cs) {
+            if (cs != run_cs) {
+              if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
+              run_cs = cs;
+              run_lo = cd;
+            }
+            run_hi = cd;
+          }
         }
         ++dest;
       } else if (i < s.k && i < first_drop) {
         first_drop = i;
       }
     }
+    if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
   }
   if (first_drop < s.k) atomicMin(&s_first, first_drop);
   const uint32_t wsum = __reduce_add_sync(0xffffffffu, old_kept);
