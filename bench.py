@@ -68,6 +68,24 @@ WORKLOADS = {
 }
 
 
+def max_over_ranks(x: float, device: str = "cuda") -> float:
+    """The largest value of x over the ranks (x itself without a process group): every rank's
+    timed region is bracketed by the same barriers, so the slowest rank sets the job's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: float, ms_per_step: float) -> float:
+    """Whole-job throughput: the units all ranks processed (weak scaling: each rank a fixed
+    share) divided by the slowest rank's time per step."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -519,12 +537,9 @@ def run_ours(args):
     binding.evict_set_profiling(run.handles[0], False)
     for h in run.handles:
         binding.evict_sync(h)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms)
     ms_per_step = ms / args.steps
-    value = world * run.tokens_per_step / (ms_per_step / 1e3)
+    value = job_throughput(world, run.tokens_per_step, ms_per_step)
 
     # end-to-end through the host-buffer entry point (copies inside the region)
     run.setup_e2e()
@@ -542,11 +557,7 @@ def run_ours(args):
         run.step_e2e()
         b.record(stream)
     barrier()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_evs) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_evs) / args.steps)
 
     peaks, peak_kind = _peaks()
     work = algorithmic_work(run, binding)
@@ -605,7 +616,7 @@ def run_ours(args):
                        "calls_per_step": run.calls_per_step, "l2": "inputs larger than L2" if
                        args.workload in ("qfilters_stack", "long_context") else "working set may be L2-resident",
                        "parallelism": f"replica-per-gpu x{world}"},
-            "e2e": {"value": round(world * run.tokens_per_step / (e2e_ms / 1e3), 1), "unit": UNIT,
+            "e2e": {"value": round(job_throughput(world, run.tokens_per_step, e2e_ms), 1), "unit": UNIT,
                     "h2d_bytes_per_step": run.h2d, "d2h_bytes_per_step": run.d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": int(launches),
             "roofline": roof,
