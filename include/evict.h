@@ -177,9 +177,11 @@ int evict_update_and_fetch_group(evict_handle* const* handles, int n_layers, con
 
 /* Same as evict_update_and_fetch with HOST inputs: copies k_host, v_host
  * (and pos_host if not NULL) to library staging buffers with one
- * cudaMemcpyAsync each on the handle's stream, then runs the update.
- * Host buffers should be pinned; they must stay valid until the stream
- * passes the call. */
+ * cudaMemcpyAsync each on a copy stream of the handle, which the handle's
+ * stream then waits for before the update (events on both sides order the
+ * staging buffers, so successive calls on different handles overlap one
+ * call's kernels with the next call's copies). Host buffers should be
+ * pinned; they must stay valid until the handle's stream passes the call. */
 int evict_update_and_fetch_host(evict_handle* h, const void* k_host, const void* v_host,
                                 const int32_t* pos_host, int m, evict_view* out);
 

@@ -67,6 +67,10 @@ struct evict_handle {
   void* k_stage = nullptr;
   void* v_stage = nullptr;
   int32_t* pos_stage = nullptr;
+  cudaStream_t copy_stream = nullptr;   // host-input call: copies into the staging buffers
+  cudaEvent_t stage_ready = nullptr;    // the staged block has landed (copy stream)
+  cudaEvent_t stage_free = nullptr;     // the last call's kernels are done with the staging (stream)
+  bool stage_used = false;
   void* tok_k = nullptr;      // per-token mode: the current token of every (b, h)
   void* tok_v = nullptr;
   int32_t* tok_pos = nullptr;

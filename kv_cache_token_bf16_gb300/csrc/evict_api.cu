@@ -433,19 +433,39 @@ int evict_update_and_fetch_host(evict_handle* h, const void* k_host, const void*
   int rc = check_update_args(h, k_host, v_host, pos_host, m, false);
   if (rc) return rc;
   if (m > 0) {
+    // The copies run on the handle's own copy stream, so that a sequence of calls (one per
+    // layer) overlaps each call's kernels with the next call's copies; events order the
+    // staging buffers between the two streams.
+    cudaError_t e = cudaSuccess;
+    if (!h->copy_stream) {
+      if ((e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&h->stage_ready, cudaEventDisableTiming)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&h->stage_free, cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e, "creating the copy stream");
+    }
+    if (h->stage_used && (e = cudaStreamWaitEvent(h->copy_stream, h->stage_free, 0)) != cudaSuccess)
+      return cuda_fail(e, "ordering the staging buffers");
     const size_t bytes = (size_t)h->cfg.batch * h->cfg.n_kv_heads * m * kHeadDim * h->elem;
-    cudaError_t e;
-    if ((e = cudaMemcpyAsync(h->k_stage, k_host, bytes, cudaMemcpyHostToDevice, h->stream)) != cudaSuccess)
+    if ((e = cudaMemcpyAsync(h->k_stage, k_host, bytes, cudaMemcpyHostToDevice, h->copy_stream)) != cudaSuccess)
       return cuda_fail(e, "copying k to the device");
-    if ((e = cudaMemcpyAsync(h->v_stage, v_host, bytes, cudaMemcpyHostToDevice, h->stream)) != cudaSuccess)
+    if ((e = cudaMemcpyAsync(h->v_stage, v_host, bytes, cudaMemcpyHostToDevice, h->copy_stream)) != cudaSuccess)
       return cuda_fail(e, "copying v to the device");
     if (pos_host) {
       const size_t pb = (size_t)h->cfg.batch * m * sizeof(int32_t);
-      if ((e = cudaMemcpyAsync(h->pos_stage, pos_host, pb, cudaMemcpyHostToDevice, h->stream)) != cudaSuccess)
+      if ((e = cudaMemcpyAsync(h->pos_stage, pos_host, pb, cudaMemcpyHostToDevice, h->copy_stream)) != cudaSuccess)
         return cuda_fail(e, "copying positions to the device");
     }
+    if ((e = cudaEventRecord(h->stage_ready, h->copy_stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(h->stream, h->stage_ready, 0)) != cudaSuccess)
+      return cuda_fail(e, "ordering the staged block");
   }
-  return evict_update_and_fetch(h, h->k_stage, h->v_stage, pos_host ? h->pos_stage : nullptr, m, out);
+  rc = evict_update_and_fetch(h, h->k_stage, h->v_stage, pos_host ? h->pos_stage : nullptr, m, out);
+  if (rc == EVICT_OK && m > 0) {
+    cudaError_t e = cudaEventRecord(h->stage_free, h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "ordering the staging buffers");
+    h->stage_used = true;
+  }
+  return rc;
 }
 
 int evict_get_view(const evict_handle* h, evict_view* out) {
@@ -541,6 +561,12 @@ void evict_destroy(evict_handle* h) {
     cudaEventDestroy(r.stop);
   }
   for (auto ev : h->event_pool) cudaEventDestroy(ev);
+  if (h->copy_stream) {
+    cudaStreamSynchronize(h->copy_stream);
+    cudaEventDestroy(h->stage_ready);
+    cudaEventDestroy(h->stage_free);
+    cudaStreamDestroy(h->copy_stream);
+  }
   cudaFree(h->arena);
   curdkv_release(h);
   delete h;

@@ -353,3 +353,28 @@ def test_more_units_than_sms_uses_two_ctas_per_sm(method):
     gpu, ref = _pair(method, B, H, 700, max_block=3000, **kw)
     view = _feed(gpu, ref, k, v, [0, 3000, 5000], check_each=True, what="160 units")
     assert_cache_equal(view, ref, "160 units")
+
+
+def test_host_inputs_back_to_back_calls_and_layers():
+    # successive host-buffer calls reuse each handle's staging buffers; the copy stream must wait
+    # for the previous call's kernels, and one layer's kernels overlap the next layer's copies
+    from kv_cache_token_bf16_gb300 import binding
+    B, H, L = 2, 4, 3
+    data = [synth.gaussian_block(70 + l, B, H, 900) for l in range(L)]
+    cuts = [0, 400, 700, 900]
+    kw = dict(n_sink=4, recent=8, keep_low=True)
+    caches = [binding.EvictCache("knorm", B, H, budget=256, max_block=400, **kw) for _ in range(L)]
+    refs = [OracleCache("knorm", B, H, budget=256, **kw) for _ in range(L)]
+    hosts = []
+    views = [None] * L
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        for l, (k, v) in enumerate(data):
+            kh = torch.from_numpy(np.ascontiguousarray(k[:, :, a:b]).view(np.int16)).pin_memory()
+            vh = torch.from_numpy(np.ascontiguousarray(v[:, :, a:b]).view(np.int16)).pin_memory()
+            hosts.append((kh, vh))                       # kept alive until the stream passes the call
+            views[l] = binding.evict_update_and_fetch_host(caches[l].handle, kh.data_ptr(), vh.data_ptr(), None,
+                                                           b - a)
+            refs[l].update_and_fetch(k[:, :, a:b], v[:, :, a:b])
+    for c, ref, vw in zip(caches, refs, views):
+        c.sync()
+        assert_cache_equal(binding.view_tensors(vw, B, H, "bf16"), ref, "host calls")
