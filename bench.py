@@ -828,10 +828,10 @@ def main():
         args.warmup = 3
     if args.method:
         ok = {"long_context": {"knorm", "qfilters", "qfilters_fallback", "curdkv", "h2o"},
-              "decode": {"knorm", "qfilters", "qfilters_fallback"}, "curdkv_planted": {"curdkv", "h2o"}}
+              "decode": {"knorm", "qfilters", "qfilters_fallback", "curdkv", "h2o"},
+              "curdkv_planted": {"curdkv", "h2o"}}
         if args.method not in ok.get(args.workload, ()):
-            ap.error("--method: long_context takes any scorer, decode knorm / qfilters / qfilters_fallback, "
-                     "curdkv_planted curdkv / h2o")
+            ap.error("--method: long_context and decode take any scorer, curdkv_planted curdkv / h2o")
         WORKLOADS[args.workload]["method"] = args.method
     if args.per_token:
         if args.workload != "curdkv_planted":

@@ -1880,11 +1880,12 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV append launch");
     h->n_kept = n;
     h->last_evicted = false;
-  } else if (c.per_token && n == c.budget + 1) {
-    // per-token step with a full cache: one row leaves, the argmin rule on ties
+  } else if (n == c.budget + 1 && m <= evict1_max_block()) {
+    // exactly one row leaves (decode steps): the fused single eviction on the pipeline's scores;
+    // the per-token mode takes the argmin rule on ties, the block form keeps the lower index
     GroupParams P = make_group_params(h, m, 1);
     P.L[0] = make_layer_ptrs(h, k, v, pos);
-    P.s.tie_low = 1;
+    P.s.tie_low = c.per_token ? 1 : 0;
     e = timed_launch(h, kKidEvict1, [&] { return launch_evict1(P, 2, sm); });
     if (e != cudaSuccess) return cuda_fail(e, "single-eviction kernel launch");
     h->n_kept = c.budget;
