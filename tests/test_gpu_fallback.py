@@ -19,7 +19,7 @@ import pytest
 from kv_cache_token_bf16_gb300 import synth
 from oracle import calibrate as ocal
 from oracle.cache import OracleCache
-from tests.gpu_util import assert_cache_equal, to_dev
+from tests.gpu_util import assert_cache_equal, to_bits, to_dev
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -177,3 +177,23 @@ def test_fallback_degenerate_keys():
     assert e.value.code == binding.EVICT_EDEVICE
     gpu2.update_and_fetch(to_dev(k[:, :, 12:20], torch), to_dev(v[:, :, 12:20], torch))
     gpu2.sync()
+
+
+@pytest.mark.parametrize("n,dtype", [(4096, "bf16"), (1000, "bf16"), (1500, "fp32")])
+def test_fallback_freeze_across_a_cluster(n, dtype):
+    # few units and many keys: the freeze splits each unit's rows over a cluster of CTAs
+    # (8 for 4096 keys, 3 for 1000, 5 for 1500 with 2 units) and sums the slices in rank order
+    B, H = 1, 2
+    k, v, axes = synth.dominant_axis_block(90 + n, B, H, n + 16, dtype=dtype)
+    gpu, ref = _pair(B, H, 256, 128, dtype=dtype, max_block=n, n_sink=4, recent=2)
+    assert _feed(gpu, ref, k, v, [0, n, n + 16], f"cluster freeze n={n}") == n
+    _check_filters(gpu, k, n, axes)
+    # the kept rows were re-scored with the frozen filter: their stored scores are the projections
+    f = gpu.filters()
+    from oracle import scores as oscores
+    view = gpu.view()
+    pos = view[2].cpu().numpy()
+    for h in range(H):
+        want = oscores.projection_canonical(k[:, h:h + 1], f[:, h], 1)[0, 0]
+        got = to_bits(view[3])[0, h]
+        assert got.tobytes() == want[pos[0, h]].astype(np.float32).tobytes()
