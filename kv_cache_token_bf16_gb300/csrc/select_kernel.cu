@@ -442,6 +442,9 @@ cudaError_t launch_select(const GroupParams& P, cudaStream_t st) {
       return launch(select_kernel<512, 16, 2>, grid, dim3(512), 0, st, P);
   }
   if (n <= 1024 * 8) return launch(select_kernel<1024, 8>, grid, dim3(1024), 0, st, P);
+  // the fewest keys per thread that hold n: less serial work per pass, no register spills
+  if (n <= 1024 * 12) return launch(select_kernel<1024, 12>, grid, dim3(1024), 0, st, P);
+  if (n <= 1024 * 17) return launch(select_kernel<1024, 17>, grid, dim3(1024), 0, st, P);
   if (n <= 1024 * 24) return launch(select_kernel<1024, 24>, grid, dim3(1024), 0, st, P);
   return launch(select_smem_kernel<1024>, grid, dim3(1024), (size_t)n * sizeof(uint32_t), st, P);
 }
