@@ -126,6 +126,32 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed fp32 pairs (lane-wise round-to-nearest, the same results as two scalar operations).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// ex2 of both lanes (the special-function unit takes one value at a time)
+__device__ __forceinline__ uint64_t ex2_f2(uint64_t x) {
+  float lo, hi;
+  f2_split(x, lo, hi);
+  return f2(ex2(lo), ex2(hi));
+}
+
 
 // 8 MMAs (K = 128 in steps of 16): D[128 x 128] = A[128 x 128] * B[128 x 128]^T.
 __device__ __forceinline__ void issue_tile_mma(uint32_t tmem, uint32_t a, uint32_t b) {
@@ -428,9 +454,15 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_lse_kernel(const __
           const float m8 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
           if (m8 > -INFINITY) {
             const float nm = fmaxf(run_max, m8 * p.scale2);
-            float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // eight running sums (element c into sum c & 7), two per packed register
+            uint64_t sm2[4] = {0ull, 0ull, 0ull, 0ull};
+            const uint64_t sc2 = f2(p.scale2, p.scale2), nm2 = f2(-nm, -nm);
 #pragma unroll
-            for (int c = 0; c < 64; ++c) sm[c & 7] += ex2(fmaf(v[c], p.scale2, -nm));
+            for (int c = 0; c < 64; c += 2)
+              sm2[(c & 7) >> 1] = add_f2(sm2[(c & 7) >> 1], ex2_f2(fma_f2(f2(v[c], v[c + 1]), sc2, nm2)));
+            float sm[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) f2_split(sm2[j], sm[2 * j], sm[2 * j + 1]);
             const float tot = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
             run_sum = run_sum * ex2(run_max - nm) + tot;         // ex2(-inf) = 0 on the first visible tile
             run_max = nm;
@@ -512,7 +544,7 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
       const int nq = quad_rows(p.m, u.q);
       if (g == g0 || u.kt == 0) {                  // the quad's lse2, +inf past the last query
         const int t = kQuad * kTile * u.q + tid;
-        s_lse[units & 1][tid] = t < p.m ? lse[(size_t)u.bh * p.lse_stride + t] : INFINITY;
+        s_lse[units & 1][tid] = t < p.m ? -lse[(size_t)u.bh * p.lse_stride + t] : -INFINITY;   // negated
         ++units;
         tc::named_sync(1, kSoftWarps * 32);
       }
@@ -529,29 +561,36 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
         tc::fence_after_sync();
         const int tq = kQuad * kTile * u.q + kTile * a;            // first query of the accumulator
         const bool full = kept || kTile * (u.kt - s.C) + kTile - 1 + p.self_excluded <= tq;
-        float sm[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t s01 = 0ull, s23 = 0ull;                  // sums of columns c & 3 = 0, 1 and 2, 3
+        const uint64_t sc2 = f2(p.scale2, p.scale2);
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
           float v[64];
           load64(acc + (uint32_t)(64 * hf), v);
-          const float* lh = l + 64 * hf;
+          const float* lh = l + 64 * hf;                  // negated lse2 of the columns
           if (full) {
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
               const float4 l4 = *reinterpret_cast<const float4*>(lh + c);
-              sm[0] += ex2(fmaf(v[c], p.scale2, -l4.x));
-              sm[1] += ex2(fmaf(v[c + 1], p.scale2, -l4.y));
-              sm[2] += ex2(fmaf(v[c + 2], p.scale2, -l4.z));
-              sm[3] += ex2(fmaf(v[c + 3], p.scale2, -l4.w));
+              s01 = add_f2(s01, ex2_f2(fma_f2(f2(v[c], v[c + 1]), sc2, f2(l4.x, l4.y))));
+              s23 = add_f2(s23, ex2_f2(fma_f2(f2(v[c + 2], v[c + 3]), sc2, f2(l4.z, l4.w))));
             }
           } else {
             // columns c >= first_t see key i (H2O: from the query after its own)
             const int first_t = i - p.k - tq - 64 * hf + p.self_excluded;
+            float sm[4];
+            f2_split(s01, sm[0], sm[1]);
+            f2_split(s23, sm[2], sm[3]);
 #pragma unroll
             for (int c = 0; c < 64; ++c)
-              if (c >= first_t) sm[c & 3] += ex2(fmaf(v[c], p.scale2, -lh[c]));
+              if (c >= first_t) sm[c & 3] += ex2(fmaf(v[c], p.scale2, lh[c]));
+            s01 = f2(sm[0], sm[1]);
+            s23 = f2(sm[2], sm[3]);
           }
         }
+        float sm[4];
+        f2_split(s01, sm[0], sm[1]);
+        f2_split(s23, sm[2], sm[3]);
         part = (sm[0] + sm[1]) + (sm[2] + sm[3]);
         tc::fence_before_sync();
         __syncwarp();
