@@ -437,6 +437,11 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_lse_kernel(const __
         for (int hf = 0; hf < 2; ++hf) {
           float v[64];
           load64(acc + (uint32_t)(64 * hf), v);
+          if (hf == 1) {                                  // the accumulator is in registers: release it
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&b.acc_empty[a]);
+          }
           if (!full) {
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
@@ -468,9 +473,6 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_lse_kernel(const __
             run_max = nm;
           }
         }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&b.acc_empty[a]);
       }
       if (u.kt == u.tiles - 1 || g == g1 - 1) {                   // this CTA's part of the unit ends
         if (a < nq && !dead && t < p.m) {
@@ -567,6 +569,11 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
         for (int hf = 0; hf < 2; ++hf) {
           float v[64];
           load64(acc + (uint32_t)(64 * hf), v);
+          if (hf == 1) {                                  // the accumulator is in registers: release it
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&b.acc_empty[a]);
+          }
           const float* lh = l + 64 * hf;                  // negated lse2 of the columns
           if (full) {
 #pragma unroll
@@ -592,9 +599,6 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
         f2_split(s01, sm[0], sm[1]);
         f2_split(s23, sm[2], sm[3]);
         part = (sm[0] + sm[1]) + (sm[2] + sm[3]);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&b.acc_empty[a]);
       }
       s_part[j & 1][a][row] = part;
       tc::named_sync(1, kSoftWarps * 32);
