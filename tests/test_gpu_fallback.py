@@ -197,3 +197,31 @@ def test_fallback_freeze_across_a_cluster(n, dtype):
         want = oscores.projection_canonical(k[:, h:h + 1], f[:, h], 1)[0, 0]
         got = to_bits(view[3])[0, h]
         assert got.tobytes() == want[pos[0, h]].astype(np.float32).tobytes()
+
+
+def test_fallback_long_context_full_size_sampled_units():
+    # the long-context stream at full size (4 x 8 heads, 16 blocks of 8192, budget 4096): the
+    # freeze at the first block on these pure-drift keys, then every block; three sampled units
+    # are followed by oracles frozen on the GPU's filters
+    from kv_cache_token_bf16_gb300 import binding
+    B, H, blocks = 4, 8, 16
+    gpu = binding.EvictCache("qfilters", B, H, budget=4096, max_block=8192, filters=None, calib_tokens=128, n_sink=4)
+    units = [(0, 0), (1, 5), (3, 7)]
+    refs = {u: OracleCache("qfilters", 1, 1, budget=4096, n_sink=4, filters=None, calib_tokens=128) for u in units}
+    for blk in range(blocks):
+        k, v = synth.long_context_block(blk, B, H)
+        view = gpu.update_and_fetch(to_dev(k, torch), to_dev(v, torch))
+        gpu.sync()
+        if blk == 0:
+            f = gpu.filters()
+            assert f is not None and np.allclose(np.linalg.norm(f, axis=-1), 1.0, atol=1e-5)
+            for (b, h), ref in refs.items():
+                ref.filter_override = lambda bb, hh, f=f, b=b, h=h: f[b, h]
+        gk, gv, gp, gs = [to_bits(t) for t in view]
+        assert gp.shape[2] == min(4096, 8192 * (blk + 1))
+        for (b, h), ref in refs.items():
+            ref.update_and_fetch(k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1])
+            assert np.array_equal(gp[b, h], ref.pos[0, 0]), (blk, b, h)
+            assert np.array_equal(gk[b, h], ref.k[0, 0]) and np.array_equal(gv[b, h], ref.v[0, 0])
+            assert gs[b, h].tobytes() == ref.score[0, 0].tobytes()
+    assert gpu.stats()["offset"] == blocks * 8192

@@ -41,8 +41,9 @@ def _gpu_mass(cache, B, H):
     return attn.cpu().numpy().astype(np.float64), inc.cpu().numpy().astype(np.float64)
 
 
-def _run_block(B, H, budget, k_old, v_old, cum_old, k_new, v_new, n_sink=4, recent=0):
-    """One GPU update from the oracle-provided state; checks every unit. Returns the GPU kept positions."""
+def _run_block(B, H, budget, k_old, v_old, cum_old, k_new, v_new, n_sink=4, recent=0, units=None):
+    """One GPU update from the oracle-provided state; checks every (or the listed) unit. Returns the GPU
+    kept positions."""
     from kv_cache_token_bf16_gb300 import binding
     k0, m = k_old.shape[2], k_new.shape[2]
     gpu = binding.EvictCache("h2o", B, H, budget=budget, n_sink=n_sink, recent=recent, max_block=m,
@@ -61,6 +62,8 @@ def _run_block(B, H, budget, k_old, v_old, cum_old, k_new, v_new, n_sink=4, rece
     n = k0 + m
     for b in range(B):
         for h in range(H):
+            if units is not None and (b, h) not in units:
+                continue
             what = f"unit {(b, h)}"
             mass = oh2o.proxy_mass(k_all[b, h], m)
             assert np.allclose(mass_g[b, h], mass, rtol=1e-4, atol=1e-7 * m), f"{what}: mass"
@@ -123,3 +126,12 @@ def test_h2o_planted_geometry_keeps_both_classes():
         for h in range(2):
             rates.append(np.mean(p["cls"][0, h, kept[0, h, 4:]] == 2))
     assert 0.2 < np.mean(rates) < 0.8
+
+
+def test_h2o_planted_full_size_sampled_units():
+    # the planted workload at full size: 8 x 8 heads, 16384 kept rows + a 512-token block, budget 2048
+    B, H, S0, m = 8, 8, 16384, 512
+    p = synth.curdkv_planted(B, H, existing=S0, incoming=m)
+    kept = _run_block(B, H, 2048, p["k"][:, :, :S0], p["v"][:, :, :S0], np.zeros((B, H, S0)), p["k"][:, :, S0:],
+                      p["v"][:, :, S0:], units={(0, 0), (5, 3), (7, 7)})
+    assert kept.shape == (B, H, 2048) and np.all(np.diff(kept, axis=2) > 0)
