@@ -12,8 +12,16 @@ Metric: cache tokens evicted-and-compacted per second (sum over layers and
 kernel's achieved HBM GB/s against the measured copy bandwidth.
 
 Other workloads (--workload): decode (B=32, H=8, 2048 prefill then
-single-token steps, budget 512, recent 128), long_context (B=4, H=8,
-16 x 8192-token blocks, budget 4096), knorm_single (B=H=1, fp32, S=1024).
+single-token steps, budget 512, recent 128; also timed with 64 steps
+captured in one CUDA graph, the "graph" key), long_context (B=4, H=8,
+16 x 8192-token blocks, budget 4096), curdkv_planted (B=H=8, 16384 kept
+rows + a 512-token block, budget 2048; reports the class-2 retention),
+knorm_single (B=H=1, fp32, S=1024).
+
+Scorer (--method): knorm, qfilters (calibrated filters), qfilters_fallback
+(no filters: the key-SVD fallback freezes after 128 keys), curdkv, h2o, for
+the decode and long_context workloads; curdkv / h2o for curdkv_planted,
+where --per-token absorbs the block one token at a time.
 
 Arms:
   --impl ours       (default) libevict on the GPU
