@@ -551,7 +551,7 @@ def run_ours(args):
 
     # end-to-end through the host-buffer entry point (copies inside the region)
     run.setup_e2e()
-    for _ in range(min(args.warmup, 3)):
+    for _ in range(args.warmup):
         if reload:
             reload()
         run.step_e2e()
