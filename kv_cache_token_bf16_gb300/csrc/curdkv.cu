@@ -126,32 +126,41 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Packed fp32 pairs (lane-wise round-to-nearest, the same results as two scalar operations).
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
+// Packed fp32 pairs: one instruction for two lanes of arithmetic, each lane rounded to nearest
+// exactly as the scalar operation would be.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
 }
-__device__ __forceinline__ void f2_split(uint64_t x, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+__device__ __forceinline__ void split_f32x2(uint64_t x, float& lo, float& hi) {
+  lo = __uint_as_float((uint32_t)x);
+  hi = __uint_as_float((uint32_t)(x >> 32));
 }
-__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-// ex2 of both lanes (the special-function unit takes one value at a time)
-__device__ __forceinline__ uint64_t ex2_f2(uint64_t x) {
-  float lo, hi;
-  f2_split(x, lo, hi);
-  return f2(ex2(lo), ex2(hi));
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
-
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// ex2 of both lanes (the special-function unit takes one value at a time)
+__device__ __forceinline__ uint64_t ex2_f32x2(uint64_t x) {
+  float lo, hi;
+  split_f32x2(x, lo, hi);
+  return pack_f32x2(ex2(lo), ex2(hi));
+}
 
 // 8 MMAs (K = 128 in steps of 16): D[128 x 128] = A[128 x 128] * B[128 x 128]^T.
 __device__ __forceinline__ void issue_tile_mma(uint32_t tmem, uint32_t a, uint32_t b) {
@@ -461,13 +470,13 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_lse_kernel(const __
             const float nm = fmaxf(run_max, m8 * p.scale2);
             // eight running sums (element c into sum c & 7), two per packed register
             uint64_t sm2[4] = {0ull, 0ull, 0ull, 0ull};
-            const uint64_t sc2 = f2(p.scale2, p.scale2), nm2 = f2(-nm, -nm);
+            const uint64_t sc2 = pack_f32x2(p.scale2, p.scale2), nm2 = pack_f32x2(-nm, -nm);
 #pragma unroll
             for (int c = 0; c < 64; c += 2)
-              sm2[(c & 7) >> 1] = add_f2(sm2[(c & 7) >> 1], ex2_f2(fma_f2(f2(v[c], v[c + 1]), sc2, nm2)));
+              sm2[(c & 7) >> 1] = add_f32x2(sm2[(c & 7) >> 1], ex2_f32x2(fma_f32x2(pack_f32x2(v[c], v[c + 1]), sc2, nm2)));
             float sm[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) f2_split(sm2[j], sm[2 * j], sm[2 * j + 1]);
+            for (int j = 0; j < 4; ++j) split_f32x2(sm2[j], sm[2 * j], sm[2 * j + 1]);
             const float tot = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
             run_sum = run_sum * ex2(run_max - nm) + tot;         // ex2(-inf) = 0 on the first visible tile
             run_max = nm;
@@ -564,7 +573,7 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
         const int tq = kQuad * kTile * u.q + kTile * a;            // first query of the accumulator
         const bool full = kept || kTile * (u.kt - s.C) + kTile - 1 + p.self_excluded <= tq;
         uint64_t s01 = 0ull, s23 = 0ull;                  // sums of columns c & 3 = 0, 1 and 2, 3
-        const uint64_t sc2 = f2(p.scale2, p.scale2);
+        const uint64_t sc2 = pack_f32x2(p.scale2, p.scale2);
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
           float v[64];
@@ -579,25 +588,25 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
               const float4 l4 = *reinterpret_cast<const float4*>(lh + c);
-              s01 = add_f2(s01, ex2_f2(fma_f2(f2(v[c], v[c + 1]), sc2, f2(l4.x, l4.y))));
-              s23 = add_f2(s23, ex2_f2(fma_f2(f2(v[c + 2], v[c + 3]), sc2, f2(l4.z, l4.w))));
+              s01 = add_f32x2(s01, ex2_f32x2(fma_f32x2(pack_f32x2(v[c], v[c + 1]), sc2, pack_f32x2(l4.x, l4.y))));
+              s23 = add_f32x2(s23, ex2_f32x2(fma_f32x2(pack_f32x2(v[c + 2], v[c + 3]), sc2, pack_f32x2(l4.z, l4.w))));
             }
           } else {
             // columns c >= first_t see key i (H2O: from the query after its own)
             const int first_t = i - p.k - tq - 64 * hf + p.self_excluded;
             float sm[4];
-            f2_split(s01, sm[0], sm[1]);
-            f2_split(s23, sm[2], sm[3]);
+            split_f32x2(s01, sm[0], sm[1]);
+            split_f32x2(s23, sm[2], sm[3]);
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c >= first_t) sm[c & 3] += ex2(fmaf(v[c], p.scale2, lh[c]));
-            s01 = f2(sm[0], sm[1]);
-            s23 = f2(sm[2], sm[3]);
+            s01 = pack_f32x2(sm[0], sm[1]);
+            s23 = pack_f32x2(sm[2], sm[3]);
           }
         }
         float sm[4];
-        f2_split(s01, sm[0], sm[1]);
-        f2_split(s23, sm[2], sm[3]);
+        split_f32x2(s01, sm[0], sm[1]);
+        split_f32x2(s23, sm[2], sm[3]);
         part = (sm[0] + sm[1]) + (sm[2] + sm[3]);
       }
       s_part[j & 1][a][row] = part;
@@ -678,20 +687,6 @@ struct GramBars {
   int fail;
 };
 
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
-}
-// Packed fp32 pairs (one instruction for two lanes of arithmetic), round to nearest.
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
   const __nv_bfloat162 b = __floats2bfloat162_rn(lo_elem, hi_elem);   // .x (low half) = lo_elem
