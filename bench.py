@@ -705,7 +705,7 @@ def algorithmic_work(run, binding):
     # fused single eviction: read the incoming keys and every row's score, move
     # the rows behind the evicted one (K, V, position and score read and written)
     out["evict1"] = {"bytes": units * m * 128 * e + units * 4 * n + new * (4 * 128 * e + 12) + old * (4 * 128 * e + 16)}
-    flag_stride = -(-w["budget"] // (32 if e == 2 else 16))
+    flag_stride = -(-w["budget"] // (64 if e == 2 else 32)) + 1      # chunk flags + the chunk counter
     out["select"] = {"bytes": int(units * (4 * n + 4 * w["budget"] + 4 * flag_stride + 8))}
     if getattr(run, "freeze_rows", 0):
         # key-SVD freeze: read the keys present once; the centred Gram is 2*D*D flops per key
