@@ -104,3 +104,49 @@ def test_captured_grouped_layers():
         for s in range(steps):
             ref.update_and_fetch(k[:, :, 100 + s:101 + s], v[:, :, 100 + s:101 + s])
         assert_cache_equal(c.view(), ref, "captured grouped step")
+
+
+@pytest.mark.parametrize("method,kw,m", [
+    ("curdkv", {}, 1),                               # decode steps: the fused single-eviction kernel
+    ("curdkv", {}, 8),                               # 8-token blocks: proxy attention, Gram, eig, leverage
+    ("h2o", {}, 1),
+    ("h2o", {}, 8),
+    ("curdkv", {"per_token": True}, 4),              # the token-by-token loop inside each call
+    ("h2o", {"per_token": True}, 4),
+    ("qfilters", {"filters": None, "calib_tokens": 96}, 4),   # the key-SVD freeze falls inside the capture
+])
+def test_captured_loop_equals_eager(method, kw, m):
+    # a captured loop and the same calls issued one by one give the same bits: no kernel of these
+    # scorers reduces in a run-dependent order, and nothing on the path reads device state back
+    from kv_cache_token_bf16_gb300 import binding
+    B, H, budget, prefill, steps = 2, 2, 64, 80, 12
+    keys = synth.clustered_keys(70, B, H, prefill + steps * m, spread=0.8)
+    vals = synth.planted_spectrum_values(71, B, H, prefill + steps * m, rank=4)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        pair = [binding.EvictCache(method, B, H, budget=budget, max_block=prefill, rank_cap=4,
+                                   stream=stream.cuda_stream, **kw) for _ in range(2)]
+        for c in pair:
+            c.update_and_fetch(to_dev(keys[:, :, :prefill], torch), to_dev(vals[:, :, :prefill], torch))
+        sl = [slice(prefill + s * m, prefill + (s + 1) * m) for s in range(steps)]
+        kd = [to_dev(keys[:, :, x], torch) for x in sl]
+        vd = [to_dev(vals[:, :, x], torch) for x in sl]
+    stream.synchronize()
+    eager, captured = pair
+    with torch.cuda.stream(stream):
+        for s in range(steps):
+            eager.update_and_fetch(kd[s], vd[s])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for s in range(steps):
+            binding.evict_update_and_fetch(captured.handle, kd[s].data_ptr(), vd[s].data_ptr(), None, m)
+    g.replay()
+    stream.synchronize()
+    for c in pair:
+        c.sync()
+    assert eager.stats() == captured.stats()
+    for a, b in zip(eager.view(), captured.view()):
+        assert np.array_equal(to_bits(a), to_bits(b)), f"{method} {kw} m={m}"
+    if method == "qfilters":
+        assert np.array_equal(eager.filters(), captured.filters())
+        assert eager.view()[0].shape[2] == budget
