@@ -897,11 +897,32 @@ constexpr int kBtBlocks = (kEigSteps + kBtBlock - 1) / kBtBlock;
 constexpr int kEigWarps = kEigThreads / 32;
 static_assert(kEigWarps == 4, "the eigensolver layout assumes four warps of 32 rows");
 
+// The Householder vectors are stored as packed rows: v_j is exactly zero at
+// indices <= j, so row j keeps only its float4 chunks from (j + 1) / 4 on
+// (16-byte aligned, about half of the square array). Chunk c of row j sits at
+// hv_row_base(j) + 4 (c - hv_first_chunk(j)); the chunks before it read as 0.
+__host__ __device__ constexpr int hv_first_chunk(int j) { return (j + 1) >> 2; }
+__host__ __device__ constexpr int hv_row_base(int j) {
+  // 4 * sum_{t < j} (32 - hv_first_chunk(t)), with sum_{u=1..j} floor(u / 4) in closed form
+  return 4 * (32 * j - (2 * (j >> 2) * ((j >> 2) - 1) + (j >> 2) * ((j & 3) + 1)));
+}
+constexpr int kHvFloats = hv_row_base(kEigSteps);
+static_assert(hv_row_base(1) == 128 && hv_row_base(4) == 4 * (4 * 32 - 1) && kHvFloats == 8316,
+              "packed Householder rows");
+
+__device__ __forceinline__ float4 hv_chunk(const float* hv, int j, int c) {
+  const int c0 = hv_first_chunk(j);
+  return c < c0 ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(hv + hv_row_base(j) + 4 * (c - c0));
+}
+
+// Shared memory of the eigensolver for up to kR eigenvectors: 106 KB for
+// kR = 16 (two CTAs per SM), 166 KB for kR = 32.
+template <int kR>
 struct EigSmem {
-  float hv[kEigSteps][kZPad];                      // Householder vector v_j (zeros up to index j)
-  float lu[5][kHeadDim][kCurdkvMaxRank];           // inverse-iteration LU factors, [factor][row][vector]
-  float z[kCurdkvMaxRank][kZPad];                  // eigenvectors (tridiagonal basis)
-  float zt[kHeadDim][kCurdkvMaxRank];              // the same during inverse iteration, [row][vector]
+  float hv[kHvFloats];                             // Householder vectors v_j, packed rows
+  float lu[5][kHeadDim][kR];                       // inverse-iteration LU factors, [factor][row][vector]
+  float z[kR][kZPad];                              // eigenvectors (tridiagonal basis)
+  float zt[kHeadDim][kR];                          // the same during inverse iteration, [row][vector]
   float vs[2][kHeadDim];                           // v of the step (by step parity)
   float cb[2][kHeadDim];                           // the next column before the step's update
   float pp[2][kHeadDim];                           // A v of the step
@@ -910,8 +931,8 @@ struct EigSmem {
   float vtv[kBtBlocks][kBtBlock][kBtBlock];        // v_k . v_m within a back-transform block
   float beta[kHeadDim], d[kHeadDim], e[kHeadDim];
   float2 de2[kHeadDim];                            // {d[i], e[i-1]^2} for the Sturm counts
-  float gram[kCurdkvMaxRank][kCurdkvMaxRank + 1];
-  float lam[kCurdkvMaxRank];
+  float gram[kR][kR + 1];
+  float lam[kR];
   double diag[kHeadDim];
   double trace;
   float tnorm;
@@ -979,9 +1000,11 @@ struct EigHalves {
   static constexpr int kOwnHalf = kBoth ? 0 : 1;   // half holding column j + 1
 };
 
-__global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid_constant__ CurdkvParams p) {
+template <int kR>
+__global__ void __launch_bounds__(kEigThreads, kR <= 16 ? 2 : 1)
+    curdkv_eig_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(16) unsigned char eig_raw[];
-  EigSmem& s = *reinterpret_cast<EigSmem*>(eig_raw);
+  EigSmem<kR>& s = *reinterpret_cast<EigSmem<kR>*>(eig_raw);
   const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int n = kHeadDim;
   const int r = p.rank;
@@ -1201,7 +1224,8 @@ __global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid
       v4.z = x4.z + (q0 + 2 == j1 ? delta : 0.f);
       v4.w = x4.w + (q0 + 3 == j1 ? delta : 0.f);
       *reinterpret_cast<float4*>(&s.vs[b][q0]) = v4;
-      *reinterpret_cast<float4*>(&s.hv[j][q0]) = v4;
+      if (lane >= hv_first_chunk(j))                    // the chunks before are exactly zero
+        *reinterpret_cast<float4*>(&s.hv[hv_row_base(j) + 4 * (lane - hv_first_chunk(j))]) = v4;
       if (lane == 0) {
         s.beta[j] = beta;
         s.e[j] = alpha;
@@ -1354,7 +1378,7 @@ __global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j0 + k < kEigSteps) u = *reinterpret_cast<const float4*>(&s.hv[j0 + k][4 * q + 32 * i]);
+          if (j0 + k < kEigSteps) u = hv_chunk(s.hv, j0 + k, q + 8 * i);
           hvq[k][4 * i] = u.x; hvq[k][4 * i + 1] = u.y; hvq[k][4 * i + 2] = u.z; hvq[k][4 * i + 3] = u.w;
         }
 #pragma unroll
@@ -1457,7 +1481,7 @@ __global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid
           if (k < nb) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float4 v = *reinterpret_cast<const float4*>(&s.hv[j0 + k][4 * q + 32 * i]);
+              const float4 v = hv_chunk(s.hv, j0 + k, q + 8 * i);
               acc = fmaf(v.x, y[4 * i], fmaf(v.y, y[4 * i + 1], fmaf(v.z, y[4 * i + 2], fmaf(v.w, y[4 * i + 3], acc))));
             }
           }
@@ -1480,7 +1504,7 @@ __global__ void __launch_bounds__(kEigThreads, 1) curdkv_eig_kernel(const __grid
           if (k < nb) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float4 v = *reinterpret_cast<const float4*>(&s.hv[j0 + k][4 * q + 32 * i]);
+              const float4 v = hv_chunk(s.hv, j0 + k, q + 8 * i);
               y[4 * i] = fmaf(-coef[k], v.x, y[4 * i]);
               y[4 * i + 1] = fmaf(-coef[k], v.y, y[4 * i + 1]);
               y[4 * i + 2] = fmaf(-coef[k], v.z, y[4 * i + 2]);
@@ -1796,8 +1820,12 @@ int curdkv_prepare(evict_handle* h) {
           cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_leverage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLevSmem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(curdkv_eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)sizeof(EigSmem))) != cudaSuccess)
+      (e = cudaFuncSetAttribute(curdkv_eig_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(EigSmem<16>))) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_eig_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_eig_kernel<kCurdkvMaxRank>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(EigSmem<kCurdkvMaxRank>))) != cudaSuccess)
     return cuda_fail(e, "CurDKV kernel attributes");
   return EVICT_OK;
 }
@@ -1899,7 +1927,10 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
     });
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV Gram launch");
     e = timed_launch(h, kKidCurdkvEig, [&] {
-      curdkv_eig_kernel<<<bh, kEigThreads, sizeof(EigSmem), sm>>>(p);
+      if (p.rank <= 16)
+        curdkv_eig_kernel<16><<<bh, kEigThreads, sizeof(EigSmem<16>), sm>>>(p);
+      else
+        curdkv_eig_kernel<kCurdkvMaxRank><<<bh, kEigThreads, sizeof(EigSmem<kCurdkvMaxRank>), sm>>>(p);
       return cudaGetLastError();
     });
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV eigensolver launch");

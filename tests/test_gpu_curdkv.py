@@ -37,10 +37,10 @@ def _built():
         pytest.skip("no CUDA device")
 
 
-def _gpu_cache(B, H, budget, max_block, max_kept=0, n_sink=4, recent=0):
+def _gpu_cache(B, H, budget, max_block, max_kept=0, n_sink=4, recent=0, rank=RANK):
     from kv_cache_token_bf16_gb300 import binding
     return binding.EvictCache("curdkv", B, H, budget=budget, n_sink=n_sink, recent=recent, max_block=max_block,
-                              max_kept=max_kept, rank_cap=RANK)
+                              max_kept=max_kept, rank_cap=rank)
 
 
 def _gpu_scores(cache, B, H):
@@ -54,13 +54,13 @@ def _gpu_scores(cache, B, H):
 
 
 def _check_unit(k_all, v_all, m, attn_g, lev_g, cum_old, cum_g_all, kept_g, n_sink, recent, budget, what,
-                assert_lev=True):
+                assert_lev=True, rank=RANK):
     """Compare one (b, h) unit with the oracle; returns the rank-r relative gap."""
-    l_or, a_or, s = ocd.block_scores(k_all, v_all, m, RANK)
+    l_or, a_or, s = ocd.block_scores(k_all, v_all, m, rank)
     n = len(l_or)
     assert np.allclose(attn_g, a_or, rtol=1e-4, atol=1e-7 * m), f"{what}: attention sums"
     lam = s ** 2
-    r = min(RANK, n, 128)
+    r = min(rank, n, 128)
     gap = (lam[r - 1] - lam[r]) / lam[0] if lam[0] > 0 and r < len(lam) else 1.0
     tol = 1e-3 * l_or + 1e-9 * l_or.sum()
     assert abs(lev_g.sum() - l_or.sum()) <= 1e-4 * l_or.sum() + 1e-12, f"{what}: captured energy"
@@ -85,11 +85,11 @@ def _check_unit(k_all, v_all, m, attn_g, lev_g, cum_old, cum_g_all, kept_g, n_si
 
 
 def _run_block(B, H, budget, k_old, v_old, cum_old, k_new, v_new, n_sink=4, recent=0, assert_lev=True,
-               units=None):
+               units=None, rank=RANK):
     """One GPU update starting from the oracle-provided state; checks every (or the listed) unit."""
     k0 = k_old.shape[2]
     m = k_new.shape[2]
-    gpu = _gpu_cache(B, H, budget, max_block=m, max_kept=max(k0, budget), n_sink=n_sink, recent=recent)
+    gpu = _gpu_cache(B, H, budget, max_block=m, max_kept=max(k0, budget), n_sink=n_sink, recent=recent, rank=rank)
     if k0:
         pos0 = np.broadcast_to(np.arange(k0, dtype=np.int32), (B, H, k0)).copy()
         gpu.set_state(to_dev(k_old, torch), to_dev(v_old, torch), torch.from_numpy(pos0).cuda(),
@@ -110,7 +110,7 @@ def _run_block(B, H, budget, k_old, v_old, cum_old, k_new, v_new, n_sink=4, rece
             assert np.array_equal(gk[b, h], k_all[b, h, kept]) and np.array_equal(gv[b, h], v_all[b, h, kept])
             gaps.append(_check_unit(k_all[b, h], v_all[b, h], m, attn[b, h], lev[b, h],
                                     cum_old[b, h].astype(np.float32).astype(np.float64), None, kept, n_sink,
-                                    recent, budget, f"unit {(b, h)}", assert_lev))
+                                    recent, budget, f"unit {(b, h)}", assert_lev, rank))
     return gpu, view, attn, lev, gaps
 
 
@@ -125,6 +125,20 @@ def test_planted_spectrum_block(k0, m, budget):
     gpu, view, attn, lev, gaps = _run_block(B, H, budget, k_all[:, :, :k0], v_all[:, :, :k0], cum_old,
                                             k_all[:, :, k0:], v_all[:, :, k0:])
     assert min(gaps) >= 1e-2           # the planted spectrum keeps the leverage well-conditioned
+
+
+@pytest.mark.parametrize("rank", [1, 8, 16, 17, 24, 32])
+def test_rank_caps_on_both_eigensolver_layouts(rank):
+    # ranks up to 16 run the eigensolver's small layout (two CTAs per SM), larger ranks the
+    # 32-vector one; a slower spectral decay keeps a clear gap after the r-th direction
+    B, H, k0, m, budget = 1, 3, 200, 180, 128
+    n = k0 + m
+    k_all = synth.clustered_keys(600 + rank, B, H, n, spread=0.5)
+    v_all = synth.planted_spectrum_values(700 + rank, B, H, n, rank=rank, decay=0.95)
+    cum_old = synth.rng(7).uniform(0, 0.01, (B, H, k0))
+    *_, gaps = _run_block(B, H, budget, k_all[:, :, :k0], v_all[:, :, :k0], cum_old, k_all[:, :, k0:],
+                          v_all[:, :, k0:], rank=rank)
+    assert min(gaps) >= 1e-2
 
 
 def test_append_then_evict_accumulates_leverage():
