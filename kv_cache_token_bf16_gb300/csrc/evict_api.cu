@@ -438,10 +438,20 @@ int evict_update_and_fetch_host(evict_handle* h, const void* k_host, const void*
     // staging buffers between the two streams.
     cudaError_t e = cudaSuccess;
     if (!h->copy_stream) {
-      if ((e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking)) != cudaSuccess ||
-          (e = cudaEventCreateWithFlags(&h->stage_ready, cudaEventDisableTiming)) != cudaSuccess ||
-          (e = cudaEventCreateWithFlags(&h->stage_free, cudaEventDisableTiming)) != cudaSuccess)
+      // all three or none: a later call takes a non-null copy stream as fully set up
+      cudaStream_t cs = nullptr;
+      cudaEvent_t ready = nullptr, freed = nullptr;
+      if ((e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&freed, cudaEventDisableTiming)) != cudaSuccess) {
+        if (freed) cudaEventDestroy(freed);
+        if (ready) cudaEventDestroy(ready);
+        if (cs) cudaStreamDestroy(cs);
         return cuda_fail(e, "creating the copy stream");
+      }
+      h->copy_stream = cs;
+      h->stage_ready = ready;
+      h->stage_free = freed;
     }
     if (h->stage_used && (e = cudaStreamWaitEvent(h->copy_stream, h->stage_free, 0)) != cudaSuccess)
       return cuda_fail(e, "ordering the staging buffers");
