@@ -680,6 +680,8 @@ def algorithmic_work(run, binding):
                read/write its score (D*2 + 12 bytes per row).
     Flops / exponentials (CurDKV attention passes): 2*D per valid logit and
     one exponential per valid logit; L = sum over (b, h) of m*k + m(m+1)/2.
+    curdkv_attn_small: short blocks (m <= 8) in one kernel: every key row read
+               once (D*2 bytes) and its column sum written (4 bytes).
     curdkv_gram: 2*D*D flops per row (the bf16 hi + lo split doubles the
                tensor-core work; the algorithmic count is one product).
     evict1   : the fused single-eviction step: incoming keys, every row's
@@ -718,6 +720,9 @@ def algorithmic_work(run, binding):
             out[k] = {"flops": 2 * 128 * logits / calls, "exps": logits / calls}
         out["curdkv_gram"] = {"flops": units * n * 2 * 128 * 128}
         out["h2o_mass"] = {"bytes": int(units * n * 16)}       # read the sum, write it, read/write the score
+        # short blocks: every key read once and its column sum written (H2O adds the score update)
+        out["curdkv_attn_small"] = {"bytes": int(units * n * (128 * 2 + 4)), "flops": 2 * 128 * logits / calls,
+                                    "exps": logits / calls}
         out["curdkv_leverage"] = {"bytes": int(units * n * (128 * 2 + 12))}
     return out
 

@@ -30,6 +30,7 @@ enum KernelId : int {
   kKidEvict1,
   kKidFreeze,
   kKidH2oMass,
+  kKidCurdkvAttnSmall,
   kKidCount
 };
 

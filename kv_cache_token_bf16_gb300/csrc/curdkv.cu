@@ -652,6 +652,148 @@ __global__ void __launch_bounds__(256) h2o_mass_kernel(const __grid_constant__ C
 }
 
 // ---------------------------------------------------------------------------
+// Proxy attention of a short block, one CTA per (b, h): the quantities of the
+// three tensor-core passes (logits k_i . q_t / sqrt(D) in base 2, each
+// query's softmax over its rows i <= k + t, column sums a_i) computed with
+// fp32 FMAs in one kernel. A decode step has one query per unit, which would
+// fill one row of a 128-row MMA tile; here the work is one dot product per
+// key. Used when m <= kSmallAttnMaxM and the m x n logits fit shared memory;
+// kM (1, 2, 4 or 8) is m rounded up, so a decode step holds one query in
+// registers and keeps eight rows per half-warp in flight (a unit's keys are
+// read at the rate its loads in flight allow). For H2O (self_excluded) it
+// also applies the mass update of h2o_mass_kernel.
+//   1. a half-warp per key row: lane c holds elements 8c .. 8c+7 of the row
+//      and of every query, and xor shuffles sum the 16 partial products; the
+//      logits go to shared memory, [t][i].
+//   2. per query: the maximum over its rows, then the sum of 2^(l - max),
+//      the terms overwriting the logits (block reductions of all m queries at
+//      once, in a fixed order).
+//   3. per row: a_i = sum over the queries that see row i of term / sum
+//      (H2O: a new row's own query left out).
+// ---------------------------------------------------------------------------
+constexpr int kSmallAttnMaxM = 8;
+constexpr int kSmallAttnMaxLogits = 16384;       // 64 KB of fp32 logits
+constexpr int kSmallAttnThreads = 512;
+constexpr int kSmallAttnWarps = kSmallAttnThreads / 32;
+constexpr int kSmallAttnHalfWarps = kSmallAttnThreads / 16;
+
+__host__ __device__ constexpr bool small_attn_fits(int m, int n) {
+  return m >= 1 && m <= kSmallAttnMaxM && (long long)m * n <= kSmallAttnMaxLogits;
+}
+
+template <int kM>
+__global__ void __launch_bounds__(kSmallAttnThreads) curdkv_attn_small_kernel(const __grid_constant__ CurdkvParams p) {
+  static_assert(kM >= 1 && kM <= kSmallAttnMaxM, "queries per CTA");
+  extern __shared__ __align__(16) float s_term[];            // [m][n]: logits, then 2^(l - max)
+  __shared__ float s_red[kSmallAttnWarps][kSmallAttnMaxM];
+  __shared__ float s_max[kSmallAttnMaxM], s_inv[kSmallAttnMaxM];
+  const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = tid & 15, hw = tid >> 4;
+  const int m = p.m, k = p.k, n = p.n;
+  const uint4* qin = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.k_in) + (size_t)bh * m * kHeadDim);
+  const uint4* kept = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.kst) + (size_t)bh * p.cap * kHeadDim);
+  constexpr int kRowVecs = kHeadDim / 8;                    // 16-byte pieces per row
+  float q[kM][8];
+#pragma unroll
+  for (int t = 0; t < kM; ++t) {
+    if (t < m) {
+      bf16x8_to_f32(__ldg(qin + (size_t)t * kRowVecs + c), q[t]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[t][e] = 0.f;
+    }
+  }
+  // 1. logits, kRowsInFlight rows of the half-warp in flight; the trip count follows the warp's
+  // first row (2 warp), so both half-warps run every shuffle together
+  constexpr int kRowsInFlight = kM <= 2 ? 8 : 4;
+  constexpr int kStep = kSmallAttnHalfWarps * kRowsInFlight;
+  for (int i0 = hw, w0 = 2 * warp; w0 < n; i0 += kStep, w0 += kStep) {
+    uint4 r[kRowsInFlight];
+#pragma unroll
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      const int i = i0 + kSmallAttnHalfWarps * u;
+      r[u] = make_uint4(0, 0, 0, 0);
+      if (i < n) r[u] = __ldg((i < k ? kept + (size_t)i * kRowVecs : qin + (size_t)(i - k) * kRowVecs) + c);
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      const int i = i0 + kSmallAttnHalfWarps * u;
+      float x[8];
+      bf16x8_to_f32(r[u], x);
+#pragma unroll
+      for (int t = 0; t < kM; ++t) {
+        if (t < m) {
+          float d = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d = fmaf(x[e], q[t][e], d);
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+          if (c == t && i < n) s_term[t * n + i] = d * p.scale2;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // 2. per query: maximum, then the sum of the terms
+  float acc[kM];
+#pragma unroll
+  for (int t = 0; t < kM; ++t) acc[t] = -INFINITY;
+  for (int i = tid; i < n; i += kSmallAttnThreads)
+#pragma unroll
+    for (int t = 0; t < kM; ++t)
+      if (t < m && i <= k + t) acc[t] = fmaxf(acc[t], s_term[t * n + i]);
+#pragma unroll
+  for (int t = 0; t < kM; ++t) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc[t] = fmaxf(acc[t], __shfl_xor_sync(0xffffffffu, acc[t], o));
+    if (lane == 0) s_red[warp][t] = acc[t];
+  }
+  __syncthreads();
+  if (tid < m) {
+    float mx = s_red[0][tid];
+    for (int w = 1; w < kSmallAttnWarps; ++w) mx = fmaxf(mx, s_red[w][tid]);
+    s_max[tid] = mx;                                         // finite: row 0 is seen by every query
+  }
+  __syncthreads();
+#pragma unroll
+  for (int t = 0; t < kM; ++t) acc[t] = 0.f;
+  for (int i = tid; i < n; i += kSmallAttnThreads)
+#pragma unroll
+    for (int t = 0; t < kM; ++t)
+      if (t < m) {
+        const float e = i <= k + t ? exp2f(s_term[t * n + i] - s_max[t]) : 0.f;
+        s_term[t * n + i] = e;
+        acc[t] += e;
+      }
+#pragma unroll
+  for (int t = 0; t < kM; ++t) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+    if (lane == 0) s_red[warp][t] = acc[t];
+  }
+  __syncthreads();
+  if (tid < m) {
+    float sum = s_red[0][tid];
+    for (int w = 1; w < kSmallAttnWarps; ++w) sum += s_red[w][tid];
+    s_inv[tid] = 1.f / sum;                                  // >= 1: the maximum's own term
+  }
+  __syncthreads();
+  // 3. column sums (each thread reads back only the terms it wrote)
+  for (int i = tid; i < n; i += kSmallAttnThreads) {
+    float a = 0.f;
+#pragma unroll
+    for (int t = 0; t < kM; ++t)
+      if (t < m && !(p.self_excluded && i == k + t)) a = fmaf(s_term[t * n + i], s_inv[t], a);
+    p.attn[(size_t)bh * p.rows + i] = a;
+    if (p.self_excluded) {
+      p.lev[(size_t)bh * p.rows + i] = a;
+      if (i < k) p.score_st[(size_t)bh * p.cap + i] += a;
+      else p.new_score[(size_t)bh * p.new_stride + (i - k)] = a;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Gram of the weighted values on the tensor cores: G = sum_i a_i^2 v_i v_i^T.
 //
 // A cluster of S CTAs per (b, h). The unit's value rows are cut into 128-row
@@ -1820,6 +1962,14 @@ int curdkv_prepare(evict_handle* h) {
           cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_leverage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLevSmem)) !=
           cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_attn_small_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmallAttnMaxLogits * (int)sizeof(float))) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_attn_small_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmallAttnMaxLogits * (int)sizeof(float))) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_attn_small_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmallAttnMaxLogits * (int)sizeof(float))) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(curdkv_attn_small_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmallAttnMaxLogits * (int)sizeof(float))) != cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_eig_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)sizeof(EigSmem<16>))) != cudaSuccess ||
       (e = cudaFuncSetAttribute(curdkv_eig_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -1881,6 +2031,22 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
   p.sched1 = make_sched(p.k, m, bh, st.sm_count, true);
   p.sched2 = make_sched(p.k, m, bh, st.sm_count, false);
   p.colpart = p.sched2.Q > 1 ? st.colpart : st.attn;
+  if (small_attn_fits(m, n)) {
+    // short blocks (decode steps, the per-token mode): one fused pass per unit
+    e = timed_launch(h, kKidCurdkvAttnSmall, [&] {
+      const size_t smem = (size_t)m * n * sizeof(float);
+      if (m == 1)
+        curdkv_attn_small_kernel<1><<<bh, kSmallAttnThreads, smem, sm>>>(p);
+      else if (m == 2)
+        curdkv_attn_small_kernel<2><<<bh, kSmallAttnThreads, smem, sm>>>(p);
+      else if (m <= 4)
+        curdkv_attn_small_kernel<4><<<bh, kSmallAttnThreads, smem, sm>>>(p);
+      else
+        curdkv_attn_small_kernel<8><<<bh, kSmallAttnThreads, smem, sm>>>(p);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "CurDKV short-block attention launch");
+  } else {
   e = timed_launch(h, kKidCurdkvLse, [&] {
     curdkv_lse_kernel<<<p.sched1.ctas, kAttnCtaThreads, attn_smem_bytes(kLseStages), sm>>>(p);
     return cudaGetLastError();
@@ -1909,7 +2075,9 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
       return cudaGetLastError();
     });
     if (e != cudaSuccess) return cuda_fail(e, "H2O mass launch");
-  } else {
+  }
+  }
+  if (!p.self_excluded) {
     e = timed_launch(h, kKidCurdkvGram, [&] {
       cudaLaunchConfig_t lc = {};
       lc.gridDim = dim3(p.gram_cluster * bh);

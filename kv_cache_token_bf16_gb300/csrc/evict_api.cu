@@ -42,7 +42,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 const char* const kKernelNames[kKidCount] = {
     "score", "score_append", "select", "compact", "calib_gram", "calib_eig",
     "curdkv_lse", "curdkv_lse_merge", "curdkv_colsum", "curdkv_colsum_merge", "curdkv_gram", "curdkv_eig", "curdkv_leverage",
-    "evict1", "qfilters_freeze", "h2o_mass",
+    "evict1", "qfilters_freeze", "h2o_mass", "curdkv_attn_small",
 };
 
 cudaEvent_t take_event(evict_handle* h) {

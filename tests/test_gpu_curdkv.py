@@ -115,7 +115,11 @@ def _run_block(B, H, budget, k_old, v_old, cum_old, k_new, v_new, n_sink=4, rece
 
 
 @pytest.mark.parametrize("k0,m,budget", [(0, 300, 64), (0, 129, 200), (500, 257, 128), (1000, 1, 64),
-                                         (127, 128, 100), (0, 513, 100), (300, 1100, 256), (129, 640, 700)])
+                                         (127, 128, 100), (0, 513, 100), (300, 1100, 256), (129, 640, 700),
+                                         # short blocks: the fused one-CTA-per-unit attention (m <= 8 and
+                                         # m * n <= 16384), its boundary, and the tensor-core path just past it
+                                         (0, 1, 64), (600, 5, 128), (2040, 8, 512), (2041, 8, 512), (3, 8, 6),
+                                         (700, 9, 128)])
 def test_planted_spectrum_block(k0, m, budget):
     B, H = 1, 2
     n = k0 + m
