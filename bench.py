@@ -681,7 +681,9 @@ def algorithmic_work(run, binding):
     Flops / exponentials (CurDKV attention passes): 2*D per valid logit and
     one exponential per valid logit; L = sum over (b, h) of m*k + m(m+1)/2.
     curdkv_attn_small: short blocks (m <= 8) in one kernel: every key row read
-               once (D*2 bytes) and its column sum written (4 bytes).
+               once (D*2 bytes) and its column sum written (4 bytes); H2O adds
+               the increment written and the score read and written (12 bytes).
+               Rows: the call's n, or budget + 1 per launch in the per-token mode.
     curdkv_gram: 2*D*D flops per row (the bf16 hi + lo split doubles the
                tensor-core work; the algorithmic count is one product).
     evict1   : the fused single-eviction step: incoming keys, every row's
@@ -713,6 +715,12 @@ def algorithmic_work(run, binding):
         # key-SVD freeze: read the keys present once; the centred Gram is 2*D*D flops per key
         out["qfilters_freeze"] = {"bytes": units * run.freeze_rows * 128 * e,
                                   "flops": units * run.freeze_rows * 2 * 128 * 128}
+    # short blocks (m <= 8): every key row read once and its column sum written; H2O also writes
+    # the increment and reads and writes the score. A per-token launch sees the budget's rows
+    # plus its token.
+    n_small = w["budget"] + 1 if w.get("per_token") else n
+    per_row = 128 * 2 + (16 if w["method"] == "h2o" else 4)
+    out["curdkv_attn_small"] = {"bytes": int(units * n_small * per_row)}
     logits = getattr(run, "logits", None)
     if logits:
         calls = run.calls_per_step
@@ -720,9 +728,6 @@ def algorithmic_work(run, binding):
             out[k] = {"flops": 2 * 128 * logits / calls, "exps": logits / calls}
         out["curdkv_gram"] = {"flops": units * n * 2 * 128 * 128}
         out["h2o_mass"] = {"bytes": int(units * n * 16)}       # read the sum, write it, read/write the score
-        # short blocks: every key read once and its column sum written (H2O adds the score update)
-        out["curdkv_attn_small"] = {"bytes": int(units * n * (128 * 2 + 4)), "flops": 2 * 128 * logits / calls,
-                                    "exps": logits / calls}
         out["curdkv_leverage"] = {"bytes": int(units * n * (128 * 2 + 12))}
     return out
 

@@ -43,6 +43,20 @@ def test_algorithmic_bytes_of_the_stack_step():
     assert work["select"]["bytes"] == units * (4 * w["seq"] + 4 * w["budget"] + 4 * flags + 8)
 
 
+@pytest.mark.parametrize("method,per_row", [("h2o", 128 * 2 + 16), ("curdkv", 128 * 2 + 4)])
+def test_algorithmic_bytes_of_the_short_block_attention(method, per_row):
+    # a decode step: every unit reads its budget + 1 key rows once and writes their column sums
+    w = dict(bench.WORKLOADS["decode"], method=method)
+    units = w["batch"] * w["heads"]
+    work = bench.algorithmic_work(_FakeRun(w, w["budget"] + 1), _FakeBinding(0, 0))
+    assert work["curdkv_attn_small"]["bytes"] == units * (w["budget"] + 1) * per_row
+    # per-token mode: each launch sees the budget's rows plus the token, whatever the call's rows
+    w = dict(bench.WORKLOADS["curdkv_planted"], method=method, per_token=True)
+    units = w["batch"] * w["heads"]
+    work = bench.algorithmic_work(_FakeRun(w, w["existing"] + w["incoming"]), _FakeBinding(0, 0))
+    assert work["curdkv_attn_small"]["bytes"] == units * (w["budget"] + 1) * per_row
+
+
 def test_throughput_and_rank_helpers():
     assert bench.job_throughput(4, 1000.0, 2.0) == pytest.approx(2.0e6)
     assert bench.max_over_ranks(3.25, device="cpu") == 3.25
