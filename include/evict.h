@@ -202,19 +202,34 @@ int evict_get_view(const evict_handle* h, evict_view* out);
  *   k_out, v_out [B, H, budget, D], pos_out, score_out [B, H, budget]
  *              device outputs; rows [0, min(n, budget)) of each (b,h) are
  *              written in temporal order.
+ * k, v, k_out and v_out must be 16-byte aligned; pos, pos_out, score_out and
+ * cfg->filters 4-byte aligned.
  * cfg->max_block, max_kept and rank_cap are ignored; work goes on cfg->stream
  * and the call returns without synchronising.
  * Intermediate data lives in one fixed 8 MiB device array inside the library
  * (held by every GPU that loads it until process exit). A call needs
- * B*H*(4n + 4*budget + 8 + 4*(ceil(budget/chunk) + 1)) bytes of it plus small
- * rounding (chunk = 64 rows for bf16, 32 for fp32); larger calls return
+ * 256 + B*H*(4n + 4*budget + 8 + 4*(ceil(budget/chunk) + 1)) bytes of it plus
+ * small rounding (chunk = 64 rows for bf16, 32 for fp32); larger calls return
  * EVICT_ELIMIT. The first call on a device looks up the array's address with
  * that device current — make it before any stream capture. All calls on a
  * device share the array, so calls that overlap on the GPU race.
- *   EVICT_EINVAL  bad configuration (as evict_init), CurDKV, NULL pointers;
- *   EVICT_ELIMIT  scratch or row bound exceeded;  EVICT_ECUDA  launch failure. */
+ *   EVICT_EINVAL  bad configuration (as evict_init), CurDKV, NULL or
+ *                 misaligned pointers (nothing is enqueued);
+ *   EVICT_ELIMIT  scratch or row bound exceeded;  EVICT_ECUDA  launch failure.
+ * A kernel that fails on the device (a bounded wait that gave up, an index
+ * outside its bounds) sets the array's error word instead; it stays set until
+ * evict_noalloc_status reads it. */
 int evict_prefill_noalloc(const evict_config* cfg, const void* k, const void* v, const int32_t* pos, int n,
                           void* k_out, void* v_out, int32_t* pos_out, float* score_out);
+
+/* Device errors of evict_prefill_noalloc calls on the current device: the
+ * pages have no counterpart. Synchronises `stream` (cudaStream_t; pass the
+ * stream the calls were made on), then reads the error word the calls share.
+ * Returns EVICT_OK if no call's kernel has reported an error since the last
+ * status call, else EVICT_EDEVICE (with the error named in
+ * evict_last_error) and clears the word. Allocates nothing; EVICT_ECUDA if
+ * the read fails. */
+int evict_noalloc_status(void* stream);
 
 /* Byte accounting from host-side counters (never synchronises). */
 int evict_stats(const evict_handle* h, evict_stats_t* out);

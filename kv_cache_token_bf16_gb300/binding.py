@@ -79,6 +79,7 @@ _SIGNATURES = {
     "evict_kernel_times": (_I, [_P, ctypes.POINTER(EvictKernelTime), _I, ctypes.POINTER(_I)]),
     "evict_compaction_rows": (_I, [_P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "evict_prefill_noalloc": (_I, [ctypes.POINTER(EvictConfig), _P, _P, _P, _I, _P, _P, _P, _P]),
+    "evict_noalloc_status": (_I, [_P]),
     "evict_curdkv_scores": (_I, [_P, _P, _P, ctypes.POINTER(_I)]),
     "evict_qfilters_filters": (_I, [_P, _P, ctypes.POINTER(_I)]),
     "evict_launch_count": (ctypes.c_int64, []),
@@ -200,6 +201,12 @@ def evict_prefill_noalloc(cfg: EvictConfig, k_ptr, v_ptr, pos_ptr, n, k_out, v_o
     """One-shot block eviction into caller buffers with no device allocation."""
     check(load().evict_prefill_noalloc(ctypes.byref(cfg), k_ptr, v_ptr, pos_ptr, n, k_out, v_out, pos_out,
                                        score_out))
+
+
+def evict_noalloc_status(stream=None):
+    """Synchronise `stream` and raise EvictError(EVICT_EDEVICE) if a no-allocation call's kernel
+    reported an error since the last status call (the error word is then cleared)."""
+    check(load().evict_noalloc_status(stream))
 
 
 def evict_curdkv_scores(h, attn_ptr, lev_ptr) -> int:

@@ -17,6 +17,9 @@
 // made on the device — make that first call before any stream capture.
 // All calls on a device share the one array, so calls that overlap on the
 // GPU (different streams, or different host threads without ordering) race.
+// The array's first 256 bytes hold the device error word: kernels that give
+// up a bounded wait or meet an index outside its bounds set it, nothing else
+// clears it, and evict_noalloc_status reads and clears it.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -40,6 +43,11 @@ std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// The error word sits at the start of the array, at the same place for every call.
+constexpr size_t kErrWordBytes = 256;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Device address of the scratch array on the current device (set-up on first use).
 int scratch_for_current_device(void** out) {
@@ -87,17 +95,24 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
   if (n == 0) return EVICT_OK;
   if (!k || !v || !k_out || !v_out || !pos_out || !score_out)
     return fail(EVICT_EINVAL, "input and output pointers must not be NULL");
+  // 16-byte vector loads and bulk copies read k / v and write k_out / v_out; positions and scores
+  // move as 4-byte words. A misaligned buffer is refused here, before anything is enqueued.
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_out, 16) || !aligned(v_out, 16))
+    return fail(EVICT_EINVAL, "k, v, k_out and v_out must be 16-byte aligned");
+  if (!aligned(pos, 4) || !aligned(pos_out, 4) || !aligned(score_out, 4))
+    return fail(EVICT_EINVAL, "pos, pos_out and score_out must be 4-byte aligned");
+  if (c.method == EVICT_QFILTERS && !aligned(c.filters, 4)) return fail(EVICT_EINVAL, "filters must be 4-byte aligned");
   if (n > EVICT_MAX_SELECT_ROWS) return fail(EVICT_ELIMIT, "n = %d above %d rows", n, EVICT_MAX_SELECT_ROWS);
   if ((long long)c.batch * c.n_kv_heads > 65535 / kMaxGroup) return fail(EVICT_ELIMIT, "batch * n_kv_heads too large");
 
   const int elem = c.dtype == EVICT_BF16 ? 2 : 4;
   const size_t bh = (size_t)c.batch * c.n_kv_heads;
   const int flag_stride = compact_flag_slots(c.budget, elem);
-  const size_t off_src = round256(bh * n * sizeof(float));
+  const size_t off_score = kErrWordBytes;
+  const size_t off_src = off_score + round256(bh * n * sizeof(float));
   const size_t off_meta = off_src + round256(bh * c.budget * sizeof(int32_t));
   const size_t off_flags = off_meta + round256(bh * sizeof(int2));
-  const size_t off_words = off_flags + round256(bh * flag_stride * sizeof(int));
-  const size_t need = off_words + 256;
+  const size_t need = off_flags + round256(bh * flag_stride * sizeof(int));
   if (need > kNoallocScratchBytes)
     return fail(EVICT_ELIMIT, "this call needs %zu bytes of scratch; the no-allocation path has %zu", need,
                 kNoallocScratchBytes);
@@ -107,11 +122,10 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
   if (rc) return rc;
   char* s = static_cast<char*>(base);
   cudaStream_t st = static_cast<cudaStream_t>(c.stream);
-  // The error word must start at zero; everything else in the scratch is
-  // written before it is read within this call (the select kernel zeroes the
-  // compaction flags and counters).
-  cudaError_t e = cudaMemsetAsync(s + off_words, 0, 256, st);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counters");
+  // Everything past the error word is written before it is read within this call (the select
+  // kernel zeroes the compaction flags and counters). The error word starts at zero with the
+  // library and is cleared only by evict_noalloc_status, so a failure is never lost.
+  cudaError_t e = cudaSuccess;
 
   GroupParams P;
   memset(&P, 0, sizeof(P));
@@ -131,7 +145,7 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
   P.s.sign = (float)(c.method == EVICT_QFILTERS ? c.sign : 1);
   P.s.method = c.method;
   P.s.offset = 0;
-  P.err = reinterpret_cast<int*>(s + off_words);
+  P.err = reinterpret_cast<int*>(s);
   LayerPtrs& L = P.L[0];
   L.k_in = k;
   L.v_in = v;
@@ -141,7 +155,7 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
   L.pos_st = pos_out;
   L.score_st = score_out;
   L.filters = const_cast<float*>(c.filters);   // read only: no fallback freeze here
-  L.new_score = reinterpret_cast<float*>(s);
+  L.new_score = reinterpret_cast<float*>(s + off_score);
   L.src_map = reinterpret_cast<int32_t*>(s + off_src);
   L.meta = reinterpret_cast<int2*>(s + off_meta);
   L.flags = reinterpret_cast<int*>(s + off_flags);
@@ -157,4 +171,22 @@ extern "C" int evict_prefill_noalloc(const evict_config* cfg, const void* k, con
   if ((e = launch_compact(P, elem, st)) != cudaSuccess) return cuda_fail(e, "compact kernel launch");
   g_launches.fetch_add(3);
   return EVICT_OK;
+}
+
+extern "C" int evict_noalloc_status(void* stream) {
+  void* base = nullptr;
+  int rc = scratch_for_current_device(&base);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, base, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the no-allocation error word");
+  if (word == kDevOk) return EVICT_OK;
+  e = cudaMemsetAsync(base, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the no-allocation error word");
+  return fail(EVICT_EDEVICE, "a no-allocation kernel reported %s",
+              word == kDevWaitTimeout ? "a bounded wait that gave up" :
+              word == kDevBadIndex ? "an index outside its bounds" : "an error");
 }

@@ -55,7 +55,7 @@ KNORM, QFILTERS, CURDKV, H2O = "knorm", "qfilters", "curdkv", "h2o"
 class OracleCache:
     def __init__(self, method, batch, n_kv_heads, budget, n_sink=4, recent=0, keep_low=True,
                  sign=1, filters=None, rank_cap=16, head_dim=128, dtype="bf16", score_mode="canonical",
-                 calib_tokens=128, filter_override=None, per_token=False):
+                 calib_tokens=128, per_token=False):
         if method not in (KNORM, QFILTERS, CURDKV, H2O):
             raise ValueError(f"unknown method {method}")
         if n_sink < 0 or recent < 0 or budget <= 0:
@@ -90,7 +90,6 @@ class OracleCache:
         self.last_kept = None          # indices kept by the last call, [B, H, n_kept]
         self.last_leverage = None      # CurDKV: leverage of the last call's rows
         self.calib_tokens = calib_tokens
-        self.filter_override = filter_override   # tests: (b, h) -> fp32 filter used at the freeze
         self.filters_bh = None         # fallback: frozen per-(b, h) filters [B, H, D] fp32
 
     # ------------------------------------------------------------------
@@ -115,10 +114,7 @@ class OracleCache:
         f = np.empty((self.batch, self.heads, self.d), np.float32)
         for b in range(self.batch):
             for h in range(self.heads):
-                if self.filter_override is not None:
-                    f[b, h] = np.asarray(self.filter_override(b, h), np.float32)
-                else:
-                    f[b, h] = _calibrate.key_svd_filter(k_all[b, h]).astype(np.float32)
+                f[b, h] = _calibrate.key_svd_filter(k_all[b, h]).astype(np.float32)
         self.filters_bh = f
 
     def _score_new(self, k_new):
@@ -189,6 +185,7 @@ class OracleCache:
             score_all = np.concatenate([self.score, self._score_new(k_new).astype(self.score.dtype)], axis=2)
             prio = priority(score_all, keep_low=(self.method == KNORM and self.keep_low))
         self.last_scores = score_all           # every row's score before this call's selection
+        self.last_rows = (k_all, v_all, pos_all)   # the concatenation this call selected from
         select = kept_indices_argmin if self.per_token else kept_indices
         idx = select(prio, self.n_sink, self.recent, self.budget)
         self.last_kept = idx

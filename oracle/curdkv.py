@@ -80,11 +80,12 @@ def leverage(w: np.ndarray, rank_cap: int) -> np.ndarray:
 def block_scores(keys: np.ndarray, values: np.ndarray, m: int, rank_cap: int):
     """Leverage of every row after appending m rows, for one (b, h).
 
-    Returns (l [n], attn [n], singular values s of W). Large blocks use the
-    query-by-query form of the attention (same values, bounded memory).
+    Returns (l [n], attn [n], singular values s of W). Very large blocks use
+    the query-by-query form of the attention (same values, bounded memory:
+    the matrix form holds three m x n fp64 arrays).
     """
     n = keys.shape[0]
-    attn = proxy_attention(keys, m) if m * n > 2e7 else proxy_attention_block(keys, m)
+    attn = proxy_attention(keys, m) if m * n > 1.1e8 else proxy_attention_block(keys, m)
     w = attn[:, None] * to_f64(values)
     l = leverage(w, rank_cap)
     s = np.linalg.svd(w, compute_uv=False)

@@ -3,14 +3,14 @@
 Test infrastructure only.
 
 Sources: "CurDKV-adapted — Value-Aware Leverage-Score Eviction", §How it works
-step 1 (the incoming key is the proxy query; its softmax over the stored keys
-is "the same softmax formulation H2O uses") and §The honesty crux, item 4 (H2O
-seeds a newly appended token's score at exactly 0; it begins accumulating at
-the next step); "L2Norm — Intrinsic Key-Norm Eviction" and "Q-Filters —
-Query-Agnostic Projection Eviction", the method tables (H2O scores a token by
-its cumulative proxy-attention mass, a softmax over the cache); "Q-Filters",
-§Integration (H2O is run at budget and n_sink only; its accumulated score
-carries its own recency bias, so no trailing window is added by default).
+step 1 (each incoming key stands in for the query, and its softmax over the
+stored keys is the one H2O scores with) and §The honesty crux, item 4 (under
+H2O a token starts from a score of zero when it is appended and gathers mass
+only from later steps); "L2Norm — Intrinsic Key-Norm Eviction" and
+"Q-Filters — Query-Agnostic Projection Eviction", the method tables (H2O ranks
+a token by the proxy attention it has accumulated); "Q-Filters",
+§Integration (H2O runs with only a budget and sinks: its accumulated score is
+already biased toward recent tokens, so no trailing window is added).
 
 Readings (the pages describe one token at a time; the cache here takes a
 block of m tokens per call, as for CurDKV):

@@ -75,3 +75,16 @@ def test_null_arguments_are_rejected(lib):
     assert lib.evict_stats(None, None) == binding.EVICT_EINVAL
     assert lib.evict_sync(None) == binding.EVICT_EINVAL
     lib.evict_destroy(None)
+
+
+def test_no_alloc_refuses_misaligned_pointers_without_a_gpu(lib):
+    # the alignment check runs before any CUDA call, so fake addresses are safe here
+    cfg = _cfg(budget=64, max_block=0)
+    base = 0x10000
+    for k, v, ko, vo, po, so, what in ((base + 2, base, base, base, base, base, "16-byte aligned"),
+                                       (base, base, base, base + 8, base, base, "16-byte aligned"),
+                                       (base, base, base, base, base + 2, base, "4-byte aligned"),
+                                       (base, base, base, base, base, base + 1, "4-byte aligned")):
+        with pytest.raises(binding.EvictError, match=what) as e:
+            binding.evict_prefill_noalloc(cfg, k, v, None, 100, ko, vo, po, so)
+        assert e.value.code == binding.EVICT_EINVAL

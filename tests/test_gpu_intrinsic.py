@@ -269,26 +269,55 @@ def test_qfilters_layer_full_size_single_and_grouped():
 
 
 # ---------------------------------------------------------------------------
-# Decode streaming (B=32, H=8, prefill 2048 then single-token steps,
-# budget 512, n_sink 4, recent 128): full shape, first 300 steps checked
-# against the oracle every 50 steps.
+# Decode streaming (B=32, H=8, prefill 2048 then 4096 single-token steps,
+# budget 512, n_sink 4, recent 128): full shape. The first 300 steps are
+# checked against a full-width oracle every 50 steps; from there three
+# sampled (b, h) units are followed by their own oracles to the end of the
+# stream, checked every 256 steps and at the last one.
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("method", ["knorm", "qfilters"])
 def test_decode_stream(method):
-    B, H, steps = 32, 8, 300
+    B, H, steps, full_width = 32, 8, 4096, 300
     k0, v0 = synth.decode_prefill(B, H, 2048)
     ks, vs = synth.decode_steps(0, steps, B, H)
     kw = dict(n_sink=4, recent=128)
-    kw.update({"keep_low": True} if method == "knorm" else {"filters": synth.decode_filters(H), "sign": 1})
+    filt = synth.decode_filters(H)
+    kw.update({"keep_low": True} if method == "knorm" else {"filters": filt, "sign": 1})
     gpu, ref = _pair(method, B, H, 512, max_block=2048, **kw)
     _feed(gpu, ref, k0, v0, [0, 2048], check_each=True, what="prefill")
     kd, vd = to_dev(ks, torch), to_dev(vs, torch)
+    units = [(0, 0), (17, 3), (31, 7)]
+    subs = {}
     for s in range(steps):
         view = gpu.update_and_fetch(kd[s], vd[s])
-        ref.update_and_fetch(ks[s], vs[s])
-        if (s + 1) % 50 == 0:
+        if s < full_width:
+            ref.update_and_fetch(ks[s], vs[s])
+            if (s + 1) % 50 == 0:
+                gpu.sync()
+                assert_cache_equal(view, ref, f"decode step {s}")
+            if s + 1 == full_width:
+                for (b, h) in units:      # the sampled units continue on oracles of their own
+                    ukw = dict(kw)
+                    if method == "qfilters":
+                        ukw["filters"] = filt[h:h + 1]
+                    sub = OracleCache(method, 1, 1, budget=512, **ukw)
+                    sub.set_state(ref.k[b:b + 1, h:h + 1], ref.v[b:b + 1, h:h + 1], ref.pos[b:b + 1, h:h + 1],
+                                  ref.score[b:b + 1, h:h + 1], ref.offset)
+                    subs[(b, h)] = sub
+            continue
+        for (b, h), sub in subs.items():
+            sub.update_and_fetch(ks[s][b:b + 1, h:h + 1], vs[s][b:b + 1, h:h + 1])
+        if (s + 1) % 256 == 0 or s + 1 == steps:
             gpu.sync()
-            assert_cache_equal(view, ref, f"decode step {s}")
+            gk, gv, gp, gs = [to_bits(t) for t in view]
+            assert gp.shape == (B, H, 512) and np.all(np.diff(gp, axis=2) > 0)
+            assert np.all(gp[:, :, :4] == np.arange(4))
+            assert np.all(gp[:, :, -128:] == 2048 + s - 127 + np.arange(128))     # the recent window
+            for (b, h), sub in subs.items():
+                what = f"decode step {s} unit {(b, h)}"
+                assert np.array_equal(gp[b, h], sub.pos[0, 0]), what
+                assert np.array_equal(gk[b, h], sub.k[0, 0]) and np.array_equal(gv[b, h], sub.v[0, 0]), what
+                assert gs[b, h].tobytes() == sub.score[0, 0].astype(np.float32).tobytes(), what
     assert gpu.stats()["offset"] == 2048 + steps
 
 
