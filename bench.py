@@ -1,36 +1,43 @@
 """Throughput of block KV-cache eviction on GB300 through libevict.
 
-Default workload: the Q-Filters calibrated Llama-3.2-3B-like layer stack —
-28 layers, 8 KV heads (24 query heads, GQA 3), D=128, bf16, B=1, one
-8192-token prefill block per layer, budget 1024, n_sink 4. One step = the
-whole hot path over that batch: every layer's cache is reset and absorbs
-the block (score, protected top-k, order-preserving compaction). Filters
-come from the GPU calibration (uncentered query SVD) run once before timing.
+Default run (the largest single-GPU workload, every scorer): the long-context
+chunked prefill. B=4 sequences, 8 KV heads, D=128, bf16; a 131072-token
+stream arrives in 16 blocks of 8192 tokens; budget 4096, n_sink 4, recent 0.
+One step = the whole hot path over that batch for all three scorers: a KNorm
+cache (keep low), a calibrated Q-Filters cache (filters from the GPU
+calibration on the workload's queries, run once before timing) and a CurDKV
+cache (rank 16, proxy queries = each block's keys) are each reset and absorb
+the 16 blocks (score, protected top-k, order-preserving compaction).
 
-Metric: cache tokens evicted-and-compacted per second (sum over layers and
-(b, h) of the rows each call scores and selects from), with the dominant
-kernel's achieved HBM GB/s against the measured copy bandwidth.
+Metric: cache tokens evicted-and-compacted per second, summed over the
+scorers, blocks and (b, h) units (each update counts the k + m rows it
+scores and selects from), with the dominant kernel's achieved rate against
+its roofline and every scorer's whole-path fraction of its binding resource.
 
-Other workloads (--workload): decode (B=32, H=8, 2048 prefill then
-single-token steps, budget 512, recent 128; also timed with 64 steps
-captured in one CUDA graph, the "graph" key), long_context (B=4, H=8,
-16 x 8192-token blocks, budget 4096), curdkv_planted (B=H=8, 16384 kept
-rows + a 512-token block, budget 2048; reports the class-2 retention),
-knorm_single (B=H=1, fp32, S=1024).
+The same JSON line carries, under "configs", the other single-GPU workloads,
+each with its own step time, rooflines, clocks and CPU baseline:
+  qfilters_stack  28 Llama-3.2-3B-like layers (24 query / 8 KV heads), one
+                  8192-token prefill per layer, budget 1024, one grouped call;
+  decode          B=32, H=8, 2048-token prefill then single-token steps,
+                  budget 512, recent 128 (KNorm; the whole 4096-step stream is
+                  also replayed as captured CUDA graphs, "stream");
+  curdkv_planted  B=H=8, 16384 kept rows + a 512-token block, budget 2048.
 
-Scorer (--method): knorm, qfilters (calibrated filters), qfilters_fallback
-(no filters: the key-SVD fallback freezes after 128 keys), curdkv, h2o, for
-the decode and long_context workloads; curdkv / h2o for curdkv_planted,
-where --per-token absorbs the block one token at a time.
+--workload picks one of them (or knorm_single) alone; --method picks one
+scorer for long_context / decode (knorm, qfilters, qfilters_fallback, curdkv,
+h2o) or curdkv_planted (curdkv, h2o); --per-token runs curdkv_planted through
+the pages' token-by-token loop.
 
 Arms:
   --impl ours       (default) libevict on the GPU
   --impl reference  the CPU oracle (numpy), as it stands, on a bounded sample
                     of the same workload; prints the same JSON line.
 
-Multi-GPU (torchrun): every rank runs its own copy of the workload on its
-own GPU (independent units, no collective on the data path); value is the
-sum over ranks divided by the slowest rank's time ("scaling": "weak").
+Multi-GPU (torchrun): the batch is partitioned by sequence. Rank r owns rows
+4r .. 4r+3 of a global batch of 4N sequences (each row is drawn from its own
+seeded stream, so the shards are exactly the rows of the global batch); no
+collective touches the data path. value = all ranks' tokens / the slowest
+rank's time ("scaling": "weak"). The sub-records run at N=1 only.
 """
 from __future__ import annotations
 
@@ -57,18 +64,21 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 METRIC = "cache tokens evicted-and-compacted/sec per layer; achieved HBM GB/s vs roofline"
 UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 << 20          # written between timed steps where the inputs could sit in L2
+HEADLINE = "long_context"
+SUB_CONFIGS = ("qfilters_stack", "decode", "curdkv_planted")
 
 
 # ----------------------------------------------------------------------------
 # workloads
 # ----------------------------------------------------------------------------
 WORKLOADS = {
+    "long_context": dict(scorers=("knorm", "qfilters", "curdkv"), layers=1, batch=4, heads=8, block=8192,
+                         blocks=16, budget=4096, n_sink=4, recent=0, rank_cap=16, dtype="bf16"),
     "qfilters_stack": dict(method="qfilters", layers=28, batch=1, heads=8, q_heads=24, seq=8192, budget=1024,
                            n_sink=4, recent=0, dtype="bf16"),
-    "decode": dict(method="knorm", layers=1, batch=32, heads=8, prefill=2048, steps=256, budget=512, n_sink=4,
+    "decode": dict(method="knorm", layers=1, batch=32, heads=8, prefill=2048, steps=4096, budget=512, n_sink=4,
                    recent=128, dtype="bf16"),
-    "long_context": dict(method="knorm", layers=1, batch=4, heads=8, block=8192, blocks=16, budget=4096, n_sink=4,
-                         recent=0, dtype="bf16"),
     "curdkv_planted": dict(method="curdkv", layers=1, batch=8, heads=8, existing=16384, incoming=512,
                            budget=2048, n_sink=4, recent=0, rank_cap=16, dtype="bf16"),
     "knorm_single": dict(method="knorm", layers=1, batch=1, heads=1, seq=1024, budget=512, n_sink=4, recent=0,
@@ -92,6 +102,14 @@ def job_throughput(world: int, units_per_rank: float, ms_per_step: float) -> flo
     """Whole-job throughput: the units all ranks processed (weak scaling: each rank a fixed
     share) divided by the slowest rank's time per step."""
     return world * units_per_rank / (ms_per_step / 1e3)
+
+
+def rank_rows(rank: int, world: int, rows_per_rank: int):
+    """Batch rows of the global batch (rows_per_rank * world sequences) that `rank` owns:
+    a contiguous slice, disjoint across ranks, together the whole batch."""
+    if not 0 <= rank < world:
+        raise ValueError("rank outside the world")
+    return rank * rows_per_rank, rows_per_rank
 
 
 def _dist():
@@ -151,6 +169,7 @@ class ClockSampler:
                                          stdout=self.tmp, stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
+        time.sleep(0.3)                 # the first sample lands inside the region
         return self
 
     def __exit__(self, *a):
@@ -182,16 +201,19 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
-# GPU arm
+# GPU arm: one class per workload
 # ----------------------------------------------------------------------------
 class StackRun:
     """Q-Filters layer stack: 28 caches updated by one grouped call per step."""
 
+    l2_note = "inputs larger than L2 (940 MB per step)"
+
     def __init__(self, w, torch, binding, stream):
         self.w, self.torch, self.binding = w, torch, binding
         L, H, S = w["layers"], w["heads"], w["seq"]
-        self.k, self.v, self.q = [], [], []
+        self.k, self.v = [], []
         self.filters = []
+        self.calib_ms = 0.0
         for layer in range(L):
             d = synth.qfilters_layer(layer, n_q_heads=w["q_heads"], n_kv_heads=H, seq_len=S, batch=w["batch"])
             self.k.append(torch.from_numpy(d["k"].view(np.int16)).cuda().view(torch.bfloat16))
@@ -201,7 +223,7 @@ class StackRun:
             t0 = time.perf_counter()
             binding.evict_qfilters_calibrate(qd.data_ptr(), binding.EVICT_BF16, w["q_heads"], qd.shape[1], 128, H,
                                              f.data_ptr(), stream.cuda_stream)
-            self.calib_ms = (time.perf_counter() - t0) * 1e3
+            self.calib_ms += (time.perf_counter() - t0) * 1e3 / L
             self.filters.append(f)
         self.caches = [binding.EvictCache("qfilters", w["batch"], H, budget=w["budget"], n_sink=w["n_sink"],
                                           recent=w["recent"], max_block=S, filters=f, sign=1,
@@ -212,65 +234,81 @@ class StackRun:
         self.tokens_per_step = L * w["batch"] * H * S
         self.calls_per_step = 1
         self.rows_per_call = S
+        self.method = "qfilters"
 
     def step(self):
         for h in self.handles:
             self.binding.evict_reset(h)
         self.binding.evict_update_and_fetch_group(self.handles, self.kp, self.vp, None, self.w["seq"])
 
-    # end-to-end through the public host-buffer call: inputs start in pinned host memory
+    # end-to-end through the public host-buffer call: inputs start in pinned host memory, and the
+    # kept caches (K, V, positions) come back to pinned host memory
     def setup_e2e(self):
         torch = self.torch
         self.kh = [t.view(torch.int16).cpu().pin_memory() for t in self.k]
         self.vh = [t.view(torch.int16).cpu().pin_memory() for t in self.v]
-        n = self.w["batch"] * self.w["heads"] * self.w["budget"]
-        self.out_h = torch.empty((len(self.caches), n), dtype=torch.int32).pin_memory()
+        self.out = [_HostCache(torch, self.w["batch"], self.w["heads"], self.w["budget"]) for _ in self.caches]
         self.h2d = sum(t.numel() * 2 for t in self.kh) + sum(t.numel() * 2 for t in self.vh)
-        self.d2h = self.out_h.numel() * 4
+        self.d2h = sum(o.nbytes for o in self.out)
 
     def step_e2e(self):
-        torch = self.torch
         for i, h in enumerate(self.handles):
             self.binding.evict_reset(h)
             view = self.binding.evict_update_and_fetch_host(h, self.kh[i].data_ptr(), self.vh[i].data_ptr(), None,
                                                             self.w["seq"])
-            pos = self.binding.view_tensors(view, self.w["batch"], self.w["heads"], "bf16")[2]
-            self.out_h[i].copy_(pos.reshape(-1), non_blocking=True)
-
-    def score_bytes_per_launch(self):
-        w = self.w
-        return w["layers"] * w["batch"] * w["heads"] * w["seq"] * (128 * 2 + 4)
+            self.out[i].fetch(self.binding, view, self.w["batch"], self.w["heads"])
 
 
-def _scorer_kwargs(w, H, torch=None):
-    """Cache arguments of a workload's scorer (w["method"]): the library method name and
-    extra keywords. Q-Filters on the decode and long-context streams: seeded unit filters
-    (decode) or the GPU calibration on the workload's queries (long context, done by the
-    caller); qfilters_fallback: no filters, the key-SVD fallback freezing after 128 keys."""
-    meth = w["method"]
-    if meth == "qfilters_fallback":
+class _HostCache:
+    """Pinned host buffers for one kept cache (K, V bf16 bits, positions): the e2e read-back."""
+
+    def __init__(self, torch, B, H, rows):
+        self.k = torch.empty((B, H, rows, 128), dtype=torch.int16).pin_memory()
+        self.v = torch.empty_like(self.k).pin_memory()
+        self.pos = torch.empty((B, H, rows), dtype=torch.int32).pin_memory()
+        self.nbytes = 2 * self.k.numel() * 2 + self.pos.numel() * 4
+
+    def fetch(self, binding, view, B, H):
+        k, v, pos, _ = binding.view_tensors(view, B, H, "bf16")
+        import torch
+        self.k.copy_(k.view(torch.int16), non_blocking=True)
+        self.v.copy_(v.view(torch.int16), non_blocking=True)
+        self.pos.copy_(pos, non_blocking=True)
+
+
+def _scorer_kwargs(method, H, torch=None):
+    """Cache arguments of a scorer: the library method name and extra keywords. Q-Filters on the
+    decode stream: seeded unit filters; qfilters_fallback: no filters, the key-SVD fallback freezing
+    after 128 keys."""
+    if method == "qfilters_fallback":
         return "qfilters", {"filters": None, "calib_tokens": 128, "sign": 1}
-    if meth == "qfilters":
+    if method == "qfilters":
         f = synth.decode_filters(H)
         return "qfilters", {"filters": torch.from_numpy(f).cuda() if torch else f, "sign": 1}
-    if meth == "curdkv":
+    if method == "curdkv":
         return "curdkv", {"rank_cap": 16}
-    return meth, {}                     # knorm, h2o
+    return method, {}                     # knorm, h2o
 
 
 class DecodeRun:
-    """Decode streaming: after a 2048-token prefill, one step = one single-token update."""
+    """Decode streaming: after a 2048-token prefill, one step = one single-token update.
+    Before each timed step the L2 is flushed (outside the timed events), so a step reads the
+    kept cache from HBM."""
+
+    l2_note = "L2 flushed before every timed step (512 MB write outside the events)"
+    flush_l2 = True
 
     def __init__(self, w, torch, binding, stream):
         self.w, self.torch, self.binding = w, torch, binding
         B, H = w["batch"], w["heads"]
+        self.method = w["method"]
         k0, v0 = synth.decode_prefill(B, H, w["prefill"])
         self.k0 = torch.from_numpy(k0.view(np.int16)).cuda().view(torch.bfloat16)
         self.v0 = torch.from_numpy(v0.view(np.int16)).cuda().view(torch.bfloat16)
         ks, vs = synth.decode_steps(0, w["steps"], B, H)
         self.ks = torch.from_numpy(ks.view(np.int16)).cuda().view(torch.bfloat16)
         self.vs = torch.from_numpy(vs.view(np.int16)).cuda().view(torch.bfloat16)
-        meth, extra = _scorer_kwargs(w, H, torch)
+        meth, extra = _scorer_kwargs(self.method, H, torch)
         self.cache = binding.EvictCache(meth, B, H, budget=w["budget"], n_sink=w["n_sink"],
                                         recent=w["recent"], max_block=w["prefill"], stream=stream.cuda_stream,
                                         **extra)
@@ -303,55 +341,63 @@ class DecodeRun:
         pos = self.binding.view_tensors(view, self.w["batch"], self.w["heads"], "bf16")[2]
         self.out_h.copy_(pos.reshape(-1), non_blocking=True)
 
-    def score_bytes_per_launch(self):
-        w = self.w
-        return w["batch"] * w["heads"] * (128 * 2 + 4)
-
-    def graph_leg(self, stream, reps, per_graph=64):
-        """The same steps captured in one CUDA graph of `per_graph` decode steps and replayed;
-        before each replay the cache is restored to the captured start state (evict_set_state,
-        outside the timed events)."""
+    def stream_leg(self, stream, per_graph=64):
+        """The whole decode stream (every input step, in order, from the state after the prefill)
+        captured as CUDA graphs of `per_graph` single-token steps and replayed back to back; the
+        steady state keeps the kept cache in L2. Returns the per-step time over the stream."""
         torch, b = self.torch, self.binding
-        per_graph = min(per_graph, self.w["steps"])
+        steps = self.w["steps"]
+        B, H = self.w["batch"], self.w["heads"]
+        meth, extra = _scorer_kwargs(self.method, H, torch)
+        cache = b.EvictCache(meth, B, H, budget=self.w["budget"], n_sink=self.w["n_sink"], recent=self.w["recent"],
+                             max_block=self.w["prefill"], stream=stream.cuda_stream, **extra)
         with torch.cuda.stream(stream):
-            snap = [t.contiguous().clone() for t in self.cache.view()]
-        off = b.evict_stats(self.handle)["offset"]
+            cache.update_and_fetch(self.k0, self.v0)
+            snap = [t.contiguous().clone() for t in cache.view()]
+        off = b.evict_stats(cache.handle)["offset"]
         stream.synchronize()
-        g = torch.cuda.CUDAGraph()
+        graphs = []
         launches0 = b.evict_launch_count()
-        with torch.cuda.graph(g, stream=stream):
-            for s in range(per_graph):
-                b.evict_update_and_fetch(self.handle, self.ks[s].data_ptr(), self.vs[s].data_ptr(), None, 1)
+        for g0 in range(0, steps, per_graph):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(g0, min(g0 + per_graph, steps)):
+                    b.evict_update_and_fetch(cache.handle, self.ks[s].data_ptr(), self.vs[s].data_ptr(), None, 1)
+            graphs.append(g)
         launches = b.evict_launch_count() - launches0
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps + 1)]
-        with torch.cuda.stream(stream):
-            for a, e in evs:
-                b.evict_set_state(self.handle, snap[0].data_ptr(), snap[1].data_ptr(), snap[2].data_ptr(),
+        times = []
+        for rep in range(2):                   # the first pass warms up
+            with torch.cuda.stream(stream):
+                b.evict_set_state(cache.handle, snap[0].data_ptr(), snap[1].data_ptr(), snap[2].data_ptr(),
                                   snap[3].data_ptr(), snap[0].shape[2], off)
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                g.replay()
+                for g in graphs:
+                    g.replay()
                 e.record(stream)
-        stream.synchronize()
-        b.evict_sync(self.handle)
-        ms = sum(a.elapsed_time(e) for a, e in evs[1:]) / reps          # the first replay is warm-up
-        return {"steps_per_graph": per_graph, "replays": reps, "gpu_launches_per_graph": int(launches),
-                "ms_per_step": round(ms / per_graph, 5),
-                "value": round(self.tokens_per_step / (ms / per_graph / 1e3), 1), "unit": UNIT}
+            stream.synchronize()
+            times.append(a.elapsed_time(e))
+        b.evict_sync(cache.handle)
+        cache.close()
+        ms = times[-1] / steps
+        return {"steps": steps, "steps_per_graph": per_graph, "gpu_launches_per_step": launches / steps,
+                "ms_per_step": round(ms, 5), "value": round(self.tokens_per_step / (ms / 1e3), 1), "unit": UNIT,
+                "l2": "steady state: the 67 MB kept cache stays in L2 between steps"}
 
 
 class LongContextRun:
-    """Long-context chunked prefill: one step = 16 blocks of 8192 tokens through one cache."""
+    """Long-context chunked prefill through one scorer: one step = 16 blocks of 8192 tokens
+    through one cache (reset first). `inputs` are shared device blocks when several scorers run."""
 
-    def __init__(self, w, torch, binding, stream):
+    l2_note = "inputs larger than L2 (2.1 GB of blocks per scorer per step)"
+
+    def __init__(self, w, torch, binding, stream, method, inputs=None, first_row=0):
         self.w, self.torch, self.binding = w, torch, binding
+        self.method = method
         B, H = w["batch"], w["heads"]
-        self.k, self.v = [], []
-        for blk in range(w["blocks"]):
-            k, v = synth.long_context_block(blk, B, H, w["block"])
-            self.k.append(torch.from_numpy(k.view(np.int16)).cuda().view(torch.bfloat16))
-            self.v.append(torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16))
-        meth, extra = _scorer_kwargs(w, H, torch)
-        if w["method"] == "qfilters":
+        self.inputs = inputs or LongContextInputs(w, torch, first_row)
+        meth, extra = _scorer_kwargs(method, H, torch)
+        if method == "qfilters":
             q = synth.long_context_queries(H)
             qd = torch.from_numpy(q.view(np.int16)).cuda()
             f = torch.empty((H, 128), dtype=torch.float32, device="cuda")
@@ -359,54 +405,99 @@ class LongContextRun:
                                              f.data_ptr(), stream.cuda_stream)
             extra["filters"] = f
         # the fallback freezes once per sequence, on the first block (>= 128 keys)
-        self.freeze_rows = w["block"] if w["method"] == "qfilters_fallback" else 0
+        self.freeze_rows = w["block"] if method == "qfilters_fallback" else 0
         self.cache = binding.EvictCache(meth, B, H, budget=w["budget"], n_sink=w["n_sink"],
                                         recent=w["recent"], max_block=w["block"], stream=stream.cuda_stream, **extra)
         self.handle = self.cache.handle
         self.handles = [self.handle]
-        per_bh = sum(min(blk * w["block"], w["budget"]) + w["block"] for blk in range(w["blocks"]))
         kk = [min(blk * w["block"], w["budget"]) for blk in range(w["blocks"])]
         m = w["block"]
-        self.logits = B * H * sum(m * k + m * (m + 1) // 2 for k in kk)
-        self.tokens_per_step = B * H * per_bh
+        self.logits = B * H * sum(m * k + m * (m + 1) // 2 for k in kk) if method in ("curdkv", "h2o") else None
+        self.tokens_per_step = B * H * sum(k + m for k in kk)
         self.calls_per_step = w["blocks"]
-        self.rows_per_call = per_bh / w["blocks"]
+        self.rows_per_call = self.tokens_per_step / (B * H * w["blocks"])
 
     def step(self):
         self.binding.evict_reset(self.handle)
-        for k, v in zip(self.k, self.v):
+        for k, v in zip(self.inputs.k, self.inputs.v):
             self.binding.evict_update_and_fetch(self.handle, k.data_ptr(), v.data_ptr(), None, self.w["block"])
 
     def setup_e2e(self):
-        t = self.torch
-        self.kh = [x.view(t.int16).cpu().pin_memory() for x in self.k]
-        self.vh = [x.view(t.int16).cpu().pin_memory() for x in self.v]
-        self.out_h = t.empty((self.w["batch"] * self.w["heads"] * self.w["budget"],), dtype=t.int32).pin_memory()
-        self.h2d = sum(x.numel() * 2 for x in self.kh) * 2
-        self.d2h = self.out_h.numel() * 4
+        self.inputs.pin()
+        self.out = _HostCache(self.torch, self.w["batch"], self.w["heads"], self.w["budget"])
+        self.h2d = self.inputs.host_bytes
+        self.d2h = self.out.nbytes
 
     def step_e2e(self):
         self.binding.evict_reset(self.handle)
         view = None
-        for kh, vh in zip(self.kh, self.vh):
+        for kh, vh in zip(self.inputs.kh, self.inputs.vh):
             view = self.binding.evict_update_and_fetch_host(self.handle, kh.data_ptr(), vh.data_ptr(), None,
                                                             self.w["block"])
-        pos = self.binding.view_tensors(view, self.w["batch"], self.w["heads"], "bf16")[2]
-        self.out_h.copy_(pos.reshape(-1), non_blocking=True)
+        self.out.fetch(self.binding, view, self.w["batch"], self.w["heads"])
 
-    def score_bytes_per_launch(self):
-        w = self.w
-        return w["batch"] * w["heads"] * w["block"] * (128 * 2 + 4)
+
+class LongContextInputs:
+    """The 16 device blocks of the stream (and, for the end-to-end leg, pinned host copies)."""
+
+    def __init__(self, w, torch, first_row=0):
+        self.torch = torch
+        self.k, self.v = [], []
+        for blk in range(w["blocks"]):
+            k, v = synth.long_context_block(blk, w["batch"], w["heads"], w["block"], first_row=first_row)
+            self.k.append(torch.from_numpy(k.view(np.int16)).cuda().view(torch.bfloat16))
+            self.v.append(torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16))
+        self.kh = self.vh = None
+        self.host_bytes = sum(x.numel() * 2 for x in self.k) * 2
+
+    def pin(self):
+        if self.kh is None:
+            t = self.torch
+            self.kh = [x.view(t.int16).cpu().pin_memory() for x in self.k]
+            self.vh = [x.view(t.int16).cpu().pin_memory() for x in self.v]
+
+
+class LongContextSuite:
+    """Every scorer of the long-context workload over the same 16 blocks: one step = the stream
+    through each scorer's cache in turn."""
+
+    l2_note = LongContextRun.l2_note
+
+    def __init__(self, w, torch, binding, stream, first_row=0):
+        self.w = w
+        self.inputs = LongContextInputs(w, torch, first_row)
+        self.runs = [LongContextRun(w, torch, binding, stream, s, self.inputs) for s in w["scorers"]]
+        self.handles = [h for r in self.runs for h in r.handles]
+        self.tokens_per_step = sum(r.tokens_per_step for r in self.runs)
+        self.calls_per_step = sum(r.calls_per_step for r in self.runs)
+
+    def step(self):
+        for r in self.runs:
+            r.step()
+
+    def setup_e2e(self):
+        for r in self.runs:
+            r.setup_e2e()
+        self.h2d = sum(r.h2d for r in self.runs)
+        self.d2h = sum(r.d2h for r in self.runs)
+
+    def step_e2e(self):
+        for r in self.runs:
+            r.step_e2e()
 
 
 class CurdkvPlantedRun:
-    """CurDKV planted geometry: a 16384-row cache (reloaded before every step,
-    outside the timed events) absorbs a 512-token block whose keys are the
-    proxy queries; budget 2048."""
+    """CurDKV planted geometry: a 16384-row cache (reloaded before every step, outside the timed
+    events, then the L2 flushed) absorbs a 512-token block whose keys are the proxy queries;
+    budget 2048."""
+
+    l2_note = "state reloaded and L2 flushed (512 MB write) before every timed step, outside the events"
+    flush_l2 = True
 
     def __init__(self, w, torch, binding, stream):
         self.w, self.torch, self.binding = w, torch, binding
         B, H, S0, m = w["batch"], w["heads"], w["existing"], w["incoming"]
+        self.method = w["method"]
         p = synth.curdkv_planted(B, H, existing=S0, incoming=m)
         dev = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.bfloat16)
         self.k0, self.v0 = dev(p["k"][:, :, :S0]), dev(p["v"][:, :, :S0])
@@ -445,22 +536,23 @@ class CurdkvPlantedRun:
                                             self.w["incoming"])
 
     def setup_e2e(self):
-        t = self.torch
-        self.kh = self.kn.view(t.int16).cpu().pin_memory()
-        self.vh = self.vn.view(t.int16).cpu().pin_memory()
-        self.out_h = t.empty((self.w["batch"] * self.w["heads"] * self.w["budget"],), dtype=t.int32).pin_memory()
-        self.h2d, self.d2h = 2 * self.kh.numel() * 2, self.out_h.numel() * 4
+        self.kh = self.kn.view(self.torch.int16).cpu().pin_memory()
+        self.vh = self.vn.view(self.torch.int16).cpu().pin_memory()
+        self.out = _HostCache(self.torch, self.w["batch"], self.w["heads"], self.w["budget"])
+        self.h2d, self.d2h = 2 * self.kh.numel() * 2, self.out.nbytes
 
     def step_e2e(self):
         view = self.binding.evict_update_and_fetch_host(self.handle, self.kh.data_ptr(), self.vh.data_ptr(), None,
                                                         self.w["incoming"])
-        pos = self.binding.view_tensors(view, self.w["batch"], self.w["heads"], "bf16")[2]
-        self.out_h.copy_(pos.reshape(-1), non_blocking=True)
+        self.out.fetch(self.binding, view, self.w["batch"], self.w["heads"])
 
 
 class KnormSingleRun:
+    l2_note = "working set (1 MB) L2-resident: latency-bound, report absolute time"
+
     def __init__(self, w, torch, binding, stream):
         self.w, self.torch, self.binding = w, torch, binding
+        self.method = "knorm"
         k, v = synth.knorm_single_sequence(w["seq"])
         self.k, self.v = torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda()
         self.cache = binding.EvictCache("knorm", 1, 1, budget=w["budget"], n_sink=w["n_sink"], recent=0,
@@ -488,98 +580,78 @@ class KnormSingleRun:
         pos = self.binding.view_tensors(view, 1, 1, "fp32")[2]
         self.out_h.copy_(pos.reshape(-1), non_blocking=True)
 
-    def score_bytes_per_launch(self):
-        return self.w["seq"] * (128 * 4 + 4)
+
+RUNS = {"qfilters_stack": StackRun, "decode": DecodeRun, "knorm_single": KnormSingleRun,
+        "curdkv_planted": CurdkvPlantedRun}
 
 
-RUNS = {"qfilters_stack": StackRun, "decode": DecodeRun, "long_context": LongContextRun,
-        "knorm_single": KnormSingleRun, "curdkv_planted": CurdkvPlantedRun}
+def make_run(workload, w, torch, binding, stream, first_row=0):
+    if workload == "long_context":
+        if len(w["scorers"]) == 1:
+            return LongContextRun(w, torch, binding, stream, w["scorers"][0], first_row=first_row)
+        return LongContextSuite(w, torch, binding, stream, first_row)
+    return RUNS[workload](w, torch, binding, stream)
 
 
-def run_ours(args):
-    import torch
-    import torch.distributed as dist
-    world, rank, local = _dist()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    import __graft_entry__
-    __graft_entry__.build()
-    from kv_cache_token_bf16_gb300 import binding
-    stream = torch.cuda.Stream()
-    w = WORKLOADS[args.workload]
-    with torch.cuda.stream(stream):
-        run = RUNS[args.workload](w, torch, binding, stream)
-    torch.cuda.synchronize()
+# ----------------------------------------------------------------------------
+# timing
+# ----------------------------------------------------------------------------
+class Timer:
+    """CUDA events on the launching stream around each step; barriers (and a device synchronize)
+    on both sides of a region. Anything `before` does (a state reload, an L2 flush) runs outside
+    the events."""
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
+    def __init__(self, torch, stream, barrier):
+        self.torch, self.stream, self.barrier = torch, stream, barrier
 
-    reload = getattr(run, "reload", None)
-    # warm-up, on the same shapes as the timed steps
-    for _ in range(args.warmup):
-        if reload:
-            reload()
-        run.step()
-    barrier()
-    # Two timed regions of K steps each, CUDA events on the launching stream. The first gives the
-    # step time (value): events only around each step. The second, right after it, also brackets
-    # every kernel launch of the first handle with events (per-kernel times, roofline); those
-    # events make each launch wait for the previous kernel to drain, so that region's steps are
-    # slower and it is reported separately (profiled_ms_per_step).
-    def timed_steps():
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        barrier()
-        for a, b in evs:
-            if reload:
-                reload()               # restores the pre-existing cache; outside the timed events
-            a.record(stream)
-            run.step()
-            b.record(stream)
-        barrier()
+    def region(self, step, steps, before=None):
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        self.barrier()
+        with torch.cuda.stream(self.stream):
+            for a, b in evs:
+                if before:
+                    before()
+                a.record(self.stream)
+                step()
+                b.record(self.stream)
+        self.barrier()
         return sum(a.elapsed_time(b) for a, b in evs)
 
-    with ClockSampler(local) as clk:
-        launches0 = binding.evict_launch_count()
-        ms = timed_steps()
-        launches = binding.evict_launch_count() - launches0
-        binding.evict_set_profiling(run.handles[0], True)
-        profiled_ms = timed_steps()
-    ktimes = binding.evict_kernel_times(run.handles[0])
-    binding.evict_set_profiling(run.handles[0], False)
-    for h in run.handles:
-        binding.evict_sync(h)
-    ms = max_over_ranks(ms)
-    ms_per_step = ms / args.steps
-    value = job_throughput(world, run.tokens_per_step, ms_per_step)
-    profiled_ms_per_step = max_over_ranks(profiled_ms) / args.steps
 
-    # end-to-end through the host-buffer entry point (copies inside the region)
-    run.setup_e2e()
-    for _ in range(args.warmup):
+def _before(run, flush):
+    reload = getattr(run, "reload", None)
+    do_flush = flush is not None and getattr(run, "flush_l2", False)
+    if not reload and not do_flush:
+        return None
+
+    def f():
         if reload:
             reload()
-        run.step_e2e()
-    barrier()
-    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    for a, b in e2e_evs:
-        if reload:
-            reload()
-        a.record(stream)
-        run.step_e2e()
-        b.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_evs) / args.steps)
+        if do_flush:
+            flush.fill_(1)
+    return f
 
-    peaks, peak_kind = _peaks()
-    work = algorithmic_work(run, binding)
-    # the decode loop captured in a CUDA graph (one launch sequence replayed per 64 steps);
-    # after the work count, which reads the last eager update's compaction metadata
-    graph = run.graph_leg(stream, max(3, min(args.steps, 20))) if hasattr(run, "graph_leg") else None
+
+def kernel_table(run, binding, timer, steps, before):
+    """Per-kernel launches and times over a second region in which every launch of the run's
+    handles is bracketed by events (those events serialise the launches: the region is slower,
+    and its time is reported as profiled_ms_per_step)."""
+    for h in run.handles[:1] if isinstance(run, StackRun) else run.handles:
+        binding.evict_set_profiling(h, True)
+    ms = timer.region(run.step, steps, before)
+    times = {}
+    for h in run.handles[:1] if isinstance(run, StackRun) else run.handles:
+        for k, (n, t) in binding.evict_kernel_times(h).items():
+            a, b = times.get(k, (0, 0.0))
+            times[k] = (a + n, b + t)
+        binding.evict_set_profiling(h, False)
+    return ms, times
+
+
+def roofline_of(run, ktimes, work, steps, ms_per_step, peaks, peak_kind, workload):
+    """The dominant kernel against its roofline, every kernel's rate, and the whole path against
+    its binding resource."""
     kernels = {}
     tot = sum(t for _, t in ktimes.values())
     for k, (n, t) in ktimes.items():
@@ -602,68 +674,124 @@ def run_ours(args):
         wk = work.get(top, {})
         if top == "qfilters_freeze":
             achieved = wk["flops"] / (per_launch_ms / 1e3) / 1e12
-            roof = {"kernel": top, "bound": "alu", "achieved": round(achieved, 2), "peak": FP32_FMA_TFLOPS,
+            roof = {"kernel": top, "bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_FMA_TFLOPS, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / FP32_FMA_TFLOPS, 4),
+                    "algorithmic_flops_per_launch": wk["flops"]}
+        elif top in ("curdkv_lse", "curdkv_colsum", "curdkv_gram") and "flops" in wk:
+            achieved = wk["flops"] / (per_launch_ms / 1e3) / 1e12
+            roof = {"kernel": top, "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                     "algorithmic_flops_per_launch": wk["flops"]}
         elif "bytes" in wk:
             achieved = wk["bytes"] / (per_launch_ms / 1e3) / 1e9
             roof = {"kernel": top, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                     "algorithmic_bytes_per_launch": wk["bytes"]}
-        elif "flops" in wk and top in ("curdkv_lse", "curdkv_colsum"):
-            achieved = wk["flops"] / (per_launch_ms / 1e3) / 1e12
-            roof = {"kernel": top, "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                    "algorithmic_flops_per_launch": wk["flops"]}
         else:
             roof = {"kernel": top, "bound": "latency", "achieved": None, "peak": None, "unit": None, "frac": None}
         roof["peak_kind"] = peak_kind
-        roof["traffic"] = _ncu_traffic(top, args.workload)
+        roof["traffic"] = _ncu_traffic(top, workload)
         roof["avg_launch_us"] = round(per_launch_ms * 1e3, 2)
-    # the whole path: every kernel's algorithmic bytes per step over the (uninstrumented) step time,
-    # when all of the step's kernels are byte-bound
-    path = None
-    if ktimes and all("bytes" in work.get(k, {}) for k in ktimes):
-        per_step = sum(work[k]["bytes"] * n / args.steps for k, (n, _) in ktimes.items())
-        gbs = per_step / (ms_per_step / 1e3) / 1e9
-        path = {"algorithmic_bytes_per_step": int(per_step), "achieved": round(gbs, 1), "unit": "GB/s",
-                "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}
-    cpu = cpu_baseline(args.workload) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded generators standing in for real-model activations)",
-            "config": {"workload": args.workload, **{k: v for k, v in w.items()},
-                       "storage": w["dtype"], "tokens_per_step": run.tokens_per_step,
-                       "calls_per_step": run.calls_per_step, "l2": "inputs larger than L2" if
-                       args.workload in ("qfilters_stack", "long_context") else "working set may be L2-resident",
-                       "parallelism": f"replica-per-gpu x{world}"},
-            "e2e": {"value": round(job_throughput(world, run.tokens_per_step, e2e_ms), 1), "unit": UNIT,
-                    "h2d_bytes_per_step": run.h2d, "d2h_bytes_per_step": run.d2h, "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": int(launches),
-            "roofline": roof,
-            "kernels": kernels,
-            "path_roofline": path,
-            "profiled_ms_per_step": round(profiled_ms_per_step, 5),
-            "kernel_timing": "per-kernel CUDA events on the launching stream over a second timed region "
-                             "of the same K steps (profiled_ms_per_step); the step time comes from the "
-                             "first region, which has events around each step only",
-            "clocks": clk.summary(),
-            "cpu_baseline": cpu,
-        }
-        if hasattr(run, "calib_ms"):
-            line["config"]["calibration_ms_per_layer"] = round(run.calib_ms, 3)
-        if graph is not None:
-            line["graph"] = graph
-        if hasattr(run, "class2_retention"):
-            line["config"]["class2_retention"] = run.class2_retention()
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    return roof, kernels, path_roofline(run, ktimes, work, steps, ms_per_step, peaks)
 
 
+def path_roofline(run, ktimes, work, steps, ms_per_step, peaks):
+    """The whole step against its binding resource. Byte-bound paths (KNorm, Q-Filters): every
+    kernel's algorithmic bytes per step over the uninstrumented step time, against HBM. Attention
+    scorers (CurDKV, H2O): the step's ideal time is the larger of its algorithmic bytes at the HBM
+    peak and one pass of the proxy-attention products (2*D flops per logit) at the bf16 tensor
+    peak; frac = ideal / measured."""
+    if not ktimes:
+        return None
+    per_step = sum(work[k]["bytes"] * n / steps for k, (n, _) in ktimes.items() if "bytes" in work.get(k, {}))
+    logits = getattr(run, "logits", None)
+    if getattr(run, "method", None) in ("curdkv", "h2o") and logits:
+        # bytes the attention scorers must move besides the byte-bound kernels: K read for every
+        # row and, for CurDKV, V read for every row (Gram) with the cumulative score read/written
+        units_rows = run.tokens_per_step
+        extra = units_rows * (128 * 2 + (128 * 2 + 8 if run.method == "curdkv" else 8))
+        hbm_us = (per_step + extra) / (peaks["hbm_gbs"] * 1e9) * 1e6
+        flops = 2 * 128 * logits
+        tc_us = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+        ideal = max(hbm_us, tc_us)
+        return {"bound": "tensor" if tc_us >= hbm_us else "hbm", "ideal_us": round(ideal, 2),
+                "hbm_bytes_per_step": int(per_step + extra), "tensor_flops_per_step": int(flops),
+                "measured_us": round(ms_per_step * 1e3, 2), "frac": round(ideal / (ms_per_step * 1e3), 4)}
+    if not all("bytes" in work.get(k, {}) for k in ktimes):
+        return None
+    gbs = per_step / (ms_per_step / 1e3) / 1e9
+    return {"bound": "hbm", "algorithmic_bytes_per_step": int(per_step), "achieved": round(gbs, 1), "unit": "GB/s",
+            "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}
+
+
+def measure(run, workload, args, torch, binding, timer, flush, world, clocks=True, local=0, kernels=True):
+    """Warm-up, the timed step region (value), the per-kernel region (roofline; skipped with
+    kernels=False), the end-to-end region through the host-buffer entry point."""
+    before = _before(run, flush)
+    for _ in range(args.warmup):
+        if before:
+            before()
+        run.step()
+    clk = ClockSampler(local) if clocks else None
+    if clk:
+        clk.__enter__()
+    launches0 = binding.evict_launch_count()
+    ms = timer.region(run.step, args.steps, before)
+    launches = binding.evict_launch_count() - launches0
+    profiled_ms, ktimes = kernel_table(run, binding, timer, args.steps, before) if kernels else (None, {})
+    if clk:
+        clk.__exit__(None, None, None)
+    for h in run.handles:
+        binding.evict_sync(h)
+    ms_per_step = max_over_ranks(ms) / args.steps
+    peaks, peak_kind = _peaks()
+    roof, ktab, path = None, {}, None
+    if kernels:
+        work = algorithmic_work(run, binding)
+        roof, ktab, path = roofline_of(run, ktimes, work, args.steps, ms_per_step, peaks, peak_kind, workload)
+    # end-to-end through the host-buffer entry point (copies in both directions inside the region)
+    run.setup_e2e()
+    for _ in range(min(args.warmup, 3)):
+        if before:
+            before()
+        run.step_e2e()
+    e2e_ms = max_over_ranks(timer.region(run.step_e2e, args.steps, before)) / args.steps
+    rec = {
+        "value": round(job_throughput(world, run.tokens_per_step, ms_per_step), 1), "unit": UNIT,
+        "ms_per_step": round(ms_per_step, 5), "tokens_per_step": run.tokens_per_step,
+        "calls_per_step": run.calls_per_step, "gpu_launches": int(launches),
+        "l2": run.l2_note,
+        "e2e": {"value": round(job_throughput(world, run.tokens_per_step, e2e_ms), 1), "unit": UNIT,
+                "h2d_bytes_per_step": run.h2d, "d2h_bytes_per_step": run.d2h, "ms_per_step": round(e2e_ms, 4)},
+        "roofline": roof, "kernels": ktab, "path_roofline": path,
+        "profiled_ms_per_step": round(max_over_ranks(profiled_ms) / args.steps, 5) if kernels else None,
+    }
+    if clk:
+        rec["clocks"] = clk.summary()
+    return rec
+
+
+def l2_copy_probe(torch, stream):
+    """Copy bandwidth of a 2 x 24 MB working set that stays in L2 (read + write bytes, best of 20)."""
+    a = torch.empty(24 << 20, dtype=torch.uint8, device="cuda")
+    b = torch.empty_like(a)
+    best = None
+    with torch.cuda.stream(stream):
+        for i in range(25):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            b.copy_(a)
+            e1.record(stream)
+            stream.synchronize()
+            if i >= 5:
+                t = e0.elapsed_time(e1)
+                best = t if best is None else min(best, t)
+    return round(2 * a.numel() / (best / 1e3) / 1e9, 1)
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work per launch
+# ----------------------------------------------------------------------------
 def algorithmic_work(run, binding):
     """Work each kernel must do per launch (one launch covers every layer of a call).
 
@@ -692,6 +820,9 @@ def algorithmic_work(run, binding):
     qfilters_freeze : the key-SVD fallback's one-time freeze: every key present
                read once, 2*D*D fp32 flops per key for the centred Gram (bound
                by the fp32 FMA pipes, "alu").
+    A multi-block step (the long-context stream) reports averages per launch:
+    its launches see a growing kept prefix, so every figure is the step's
+    total over its launches.
     """
     w = run.w
     e = 2 if w["dtype"] == "bf16" else 4
@@ -700,6 +831,7 @@ def algorithmic_work(run, binding):
     if isinstance(run, DecodeRun):
         m = 1
     n = run.rows_per_call
+    method = getattr(run, "method", w.get("method"))
     out = {"score": {"bytes": units * m * (128 * e + 4)}}
     old, new = 0, 0
     for h in run.handles:
@@ -719,7 +851,7 @@ def algorithmic_work(run, binding):
     # the increment and reads and writes the score. A per-token launch sees the budget's rows
     # plus its token.
     n_small = w["budget"] + 1 if w.get("per_token") else n
-    per_row = 128 * 2 + (16 if w["method"] == "h2o" else 4)
+    per_row = 128 * 2 + (16 if method == "h2o" else 4)
     out["curdkv_attn_small"] = {"bytes": int(units * n_small * per_row)}
     logits = getattr(run, "logits", None)
     if logits:
@@ -729,23 +861,76 @@ def algorithmic_work(run, binding):
         out["curdkv_gram"] = {"flops": units * n * 2 * 128 * 128}
         out["h2o_mass"] = {"bytes": int(units * n * 16)}       # read the sum, write it, read/write the score
         out["curdkv_leverage"] = {"bytes": int(units * n * (128 * 2 + 12))}
+    if w.get("blocks"):
+        # the long-context stream: the compaction figures above are the last call's; average the
+        # kept rows moved and the survivors written over the step's blocks instead (the first
+        # block has no kept rows, every later one a full kept prefix of budget rows)
+        B, H = w["batch"], w["heads"]
+        blocks = w["blocks"]
+        first_new = min(w["budget"], w["block"])
+        per_unit = first_new * (4 * 128 * e + 16) + (blocks - 1) * (new * (4 * 128 * e + 16) + old * (4 * 128 * e + 20)) / (B * H)
+        out["compact"] = {"bytes": int(B * H * per_unit / blocks)}
+        n_first = w["block"]
+        n_rest = min(w["budget"], w["block"]) + w["block"]
+        n_avg = (n_first + (blocks - 1) * n_rest) / blocks
+        out["select"] = {"bytes": int(units * (4 * n_avg + 4 * w["budget"] + 4 * flag_stride + 8))}
+        if logits:
+            out["curdkv_gram"] = {"flops": int(units * n_avg * 2 * 128 * 128)}
+            out["curdkv_leverage"] = {"bytes": int(units * n_avg * (128 * 2 + 12))}
+            out["h2o_mass"] = {"bytes": int(units * n_avg * 16)}
     return out
 
 
 # ----------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 # ----------------------------------------------------------------------------
+def _oracle_long_context(w, method, budget_s):
+    """One (b, h) unit of the long-context stream through the oracle for as many blocks as fit
+    in budget_s; returns (tokens, seconds, blocks done)."""
+    from oracle import calibrate as ocal
+    from oracle.cache import OracleCache
+    meth, kw = _scorer_kwargs(method, w["heads"])
+    if method == "qfilters":
+        kw["filters"] = ocal.calibrate(synth.long_context_queries(w["heads"]), w["heads"])[:1].astype(np.float32)
+    c = OracleCache(meth, 1, 1, budget=w["budget"], n_sink=w["n_sink"], recent=w["recent"], **kw)
+    tokens, secs, done = 0, 0.0, 0
+    for blk in range(w["blocks"]):
+        k, v = synth.long_context_block(blk, 1, w["heads"], w["block"])
+        t1 = time.perf_counter()
+        n = c.n_kept + w["block"]
+        c.update_and_fetch(k[:1, :1], v[:1, :1])
+        secs += time.perf_counter() - t1
+        tokens += n
+        done += 1
+        if secs > budget_s:
+            break
+    return tokens, secs, done
+
+
 def _oracle_sample(workload, budget_s=10.0):
-    """Run the oracle on a bounded sample of the workload; returns (tokens, seconds, description)."""
+    """Run the oracle on a bounded sample of the workload; returns (tokens, seconds, description).
+    For several scorers the seconds are the whole step's estimated oracle time: each scorer's
+    sampled seconds per token times the tokens it handles in one step."""
     from oracle import calibrate as ocal
     from oracle.cache import OracleCache
     w = WORKLOADS[workload]
     tokens, secs, done = 0, 0.0, 0
+    if workload == "long_context":
+        # the step handles the same tokens with every scorer: the composite rate is the number of
+        # scorers over the sum of their seconds per token; the tokens returned are what that rate
+        # covers in the seconds actually spent
+        parts, secs, per_token = [], 0.0, 0.0
+        for method in w["scorers"]:
+            t, s, done = _oracle_long_context(w, method, budget_s / len(w["scorers"]))
+            parts.append(f"{method}: {done} block(s) of one (b, h) unit")
+            secs += s
+            per_token += s / t
+        rate = len(w["scorers"]) / per_token
+        return rate * secs, secs, "; ".join(parts) + " (composite rate: scorers / sum of seconds per token)"
     if workload == "qfilters_stack":
         t0 = time.perf_counter()
         for layer in range(w["layers"]):
             d = synth.qfilters_layer(layer, seq_len=w["seq"])
-            t1 = time.perf_counter()
             f = ocal.calibrate(d["queries"], w["heads"]).astype(np.float32)
             c = OracleCache("qfilters", w["batch"], w["heads"], budget=w["budget"], n_sink=w["n_sink"],
                             recent=w["recent"], filters=f)
@@ -759,7 +944,7 @@ def _oracle_sample(workload, budget_s=10.0):
         return tokens, secs, f"{done} of {w['layers']} layers (one prefill update each; calibration untimed)"
     if workload == "decode":
         k0, v0 = synth.decode_prefill(w["batch"], w["heads"], w["prefill"])
-        meth, kw = _scorer_kwargs(w, w["heads"])
+        meth, kw = _scorer_kwargs(w["method"], w["heads"])
         c = OracleCache(meth, w["batch"], w["heads"], budget=w["budget"], n_sink=w["n_sink"],
                         recent=w["recent"], **kw)
         c.update_and_fetch(k0, v0)
@@ -772,23 +957,6 @@ def _oracle_sample(workload, budget_s=10.0):
             if time.perf_counter() - t0 > budget_s:
                 break
         return tokens, time.perf_counter() - t0, f"{done} decode steps after the 2048-token prefill"
-    if workload == "long_context":
-        # one (b, h) unit followed through the stream (units are independent)
-        meth, kw = _scorer_kwargs(w, w["heads"])
-        if w["method"] == "qfilters":
-            kw["filters"] = ocal.calibrate(synth.long_context_queries(w["heads"]), w["heads"])[:1].astype(np.float32)
-        c = OracleCache(meth, 1, 1, budget=w["budget"], n_sink=w["n_sink"], recent=w["recent"], **kw)
-        for blk in range(w["blocks"]):
-            k, v = synth.long_context_block(blk, w["batch"], w["heads"], w["block"])
-            t1 = time.perf_counter()
-            n = c.n_kept + w["block"]
-            c.update_and_fetch(k[:1, :1], v[:1, :1])
-            secs += time.perf_counter() - t1
-            tokens += n
-            done += 1
-            if secs > budget_s:
-                break
-        return tokens, secs, f"{done} of {w['blocks']} blocks of one (b, h) unit"
     if workload == "curdkv_planted":
         S0, m = w["existing"], w["incoming"]
         p = synth.curdkv_planted(w["batch"], w["heads"], existing=S0, incoming=m)
@@ -817,10 +985,148 @@ def _oracle_sample(workload, budget_s=10.0):
     return tokens, time.perf_counter() - t0, f"{done} one-block prefills"
 
 
-def cpu_baseline(workload):
-    tokens, secs, sample = _oracle_sample(workload)
-    return {"value": round(tokens / secs, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": sample + "; numpy, single thread (the oracle's array ops do not use BLAS threads)"}
+def _oracle_threads():
+    """Threads the oracle's numpy can use: BLAS (the CurDKV SVDs and matrix products) runs on the
+    process's cores; everything else is single-threaded numpy."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(workload, budget_s=10.0):
+    tokens, secs, sample = _oracle_sample(workload, budget_s)
+    return {"value": round(tokens / secs, 1), "unit": UNIT, "cores": _oracle_threads(), "kind": "oracle",
+            "sample": sample + "; numpy (BLAS on the process's cores for the matrix products and SVDs, "
+                               "single-threaded elsewhere)"}
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+def _workload_line(name, w, rec, world, extra=None):
+    cfg = {"workload": name, **{k: (list(v) if isinstance(v, tuple) else v) for k, v in w.items()},
+           "storage": w["dtype"], "tokens_per_step": rec["tokens_per_step"], "calls_per_step": rec["calls_per_step"],
+           "l2": rec["l2"]}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from kv_cache_token_bf16_gb300 import binding
+    stream = torch.cuda.Stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    timer = Timer(torch, stream, barrier)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    w = WORKLOADS[args.workload]
+    first_row = 0
+    if args.workload == "long_context":
+        first_row, _ = rank_rows(rank, world, w["batch"])
+    with torch.cuda.stream(stream):
+        run = make_run(args.workload, w, torch, binding, stream, first_row)
+    torch.cuda.synchronize()
+    suite = isinstance(run, LongContextSuite)
+    rec = measure(run, args.workload, args, torch, binding, timer, flush, world, local=local, kernels=not suite)
+
+    extra = {"parallelism": (f"batch-row shards x{world} (rank r owns rows {w['batch']}r..{w['batch']}r+"
+                             f"{w['batch'] - 1} of {w['batch'] * world} sequences)")
+             if args.workload == "long_context" else f"replica-per-gpu x{world}"}
+    line = {
+        "metric": METRIC, "value": rec["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded generators standing in for real-model activations)",
+        "config": _workload_line(args.workload, w, rec, world, extra),
+        "e2e": dict(rec["e2e"], readback="the kept caches (K, V, positions) return to pinned host memory "
+                                         "inside the timed region" if not isinstance(run, (DecodeRun, KnormSingleRun))
+                    else "kept positions only"),
+        "gpu_launches": rec["gpu_launches"], "roofline": rec["roofline"], "kernels": rec["kernels"],
+        "path_roofline": rec["path_roofline"], "profiled_ms_per_step": rec["profiled_ms_per_step"],
+        "kernel_timing": "per-kernel CUDA events on the launching stream over a second timed region of the same "
+                         "K steps (profiled_ms_per_step; per scorer for the long-context suite); the step time "
+                         "comes from the first region, which has events around each step only",
+        "clocks": rec.get("clocks"),
+    }
+    if isinstance(run, LongContextSuite):
+        # every scorer's own stream: its step time, rooflines and kernels
+        line["scorers"] = {}
+        for sub in run.runs:
+            r = measure(sub, args.workload, args, torch, binding, timer, flush, world, clocks=False, local=local)
+            line["scorers"][sub.method] = {k: r[k] for k in ("value", "ms_per_step", "tokens_per_step", "roofline",
+                                                             "path_roofline", "kernels", "e2e",
+                                                             "profiled_ms_per_step")}
+        # the headline roofline: the step's dominant kernel (most time over all scorers)
+        tops = [(s["roofline"]["avg_launch_us"] * s["kernels"][s["roofline"]["kernel"]]["launches"], name)
+                for name, s in line["scorers"].items() if s["roofline"]]
+        if tops:
+            top = max(tops)[1]
+            line["roofline"] = dict(line["scorers"][top]["roofline"], scorer=top)
+        ideal = 0.0
+        for name, s in line["scorers"].items():
+            p = s["path_roofline"]
+            if p and "ideal_us" in p:
+                ideal += p["ideal_us"]
+            elif p:
+                ideal += p["algorithmic_bytes_per_step"] / (p["peak"] * 1e9) * 1e6
+        line["path_roofline"] = {"bound": "per scorer (HBM for KNorm / Q-Filters, tensor for CurDKV)",
+                                 "ideal_us": round(ideal, 2), "measured_us": round(rec["ms_per_step"] * 1e3, 2),
+                                 "frac": round(ideal / (rec["ms_per_step"] * 1e3), 4)}
+        line.pop("kernels")
+    if hasattr(run, "calib_ms"):
+        line["config"]["calibration_ms_per_layer"] = round(run.calib_ms, 3)
+    if hasattr(run, "class2_retention"):
+        line["config"]["class2_retention"] = run.class2_retention()
+    if isinstance(run, DecodeRun):
+        line["stream"] = run.stream_leg(stream)
+        line["stream"]["l2_copy_gbs"] = l2_copy_probe(torch, stream)
+    del run
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=15.0 if args.workload == HEADLINE else 10.0)
+    # the other single-GPU workloads, each with its own record (N=1 only)
+    if args.workload == HEADLINE and len(w["scorers"]) > 1 and world == 1 and not args.no_configs:
+        line["configs"] = {}
+        for name in SUB_CONFIGS:
+            sw = WORKLOADS[name]
+            with torch.cuda.stream(stream):
+                sub = make_run(name, sw, torch, binding, stream)
+            torch.cuda.synchronize()
+            r = measure(sub, name, args, torch, binding, timer, flush, world, local=local)
+            r["config"] = _workload_line(name, sw, r, world)
+            r.pop("l2")
+            if hasattr(sub, "calib_ms"):
+                r["config"]["calibration_ms_per_layer"] = round(sub.calib_ms, 3)
+            if hasattr(sub, "class2_retention"):
+                r["config"]["class2_retention"] = sub.class2_retention()
+            if isinstance(sub, DecodeRun):
+                r["stream"] = sub.stream_leg(stream)
+                r["stream"]["l2_copy_gbs"] = l2_copy_probe(torch, stream)
+            del sub
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            if not args.no_cpu_baseline:
+                r["cpu_baseline"] = cpu_baseline(name, budget_s=8.0)
+            line["configs"][name] = r
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
 
 
 def run_reference(args):
@@ -828,21 +1134,20 @@ def run_reference(args):
     if rank != 0:
         return
     w = WORKLOADS[args.workload]
-    vals = []
     for _ in range(args.warmup):
-        _oracle_sample(args.workload, budget_s=2.0)
+        _oracle_sample(args.workload, budget_s=1.0)
     tokens_total, secs_total, sample = 0, 0.0, ""
     for _ in range(args.steps):
-        t, s, sample = _oracle_sample(args.workload, budget_s=5.0)
+        t, s, sample = _oracle_sample(args.workload, budget_s=4.0)
         tokens_total += t
         secs_total += s
-        vals.append(t / s)
     value = tokens_total / secs_total
+    cfg = {"workload": args.workload, **{k: (list(v) if isinstance(v, tuple) else v) for k, v in w.items()}}
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs_total / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": args.workload, **w},
-            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": _oracle_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -851,14 +1156,15 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qfilters_stack")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="headline workload only (no sub-records)")
     ap.add_argument("--method", choices=["knorm", "qfilters", "qfilters_fallback", "curdkv", "h2o"], default=None,
-                    help="scorer for the long_context and decode workloads (qfilters_fallback: Q-Filters "
-                         "without calibrated filters, freezing a key-SVD filter after 128 keys) and for "
+                    help="one scorer for the long_context and decode workloads (qfilters_fallback: Q-Filters "
+                         "without calibrated filters, freezing a key-SVD filter after 128 keys) or for "
                          "curdkv_planted (curdkv or h2o)")
     ap.add_argument("--per-token", action="store_true",
                     help="curdkv_planted: absorb the incoming block one token at a time (the pages' loop)")
@@ -871,7 +1177,10 @@ def main():
               "curdkv_planted": {"curdkv", "h2o"}}
         if args.method not in ok.get(args.workload, ()):
             ap.error("--method: long_context and decode take any scorer, curdkv_planted curdkv / h2o")
-        WORKLOADS[args.workload]["method"] = args.method
+        if args.workload == "long_context":
+            WORKLOADS["long_context"]["scorers"] = (args.method,)
+        else:
+            WORKLOADS[args.workload]["method"] = args.method
     if args.per_token:
         if args.workload != "curdkv_planted":
             ap.error("--per-token applies to curdkv_planted")

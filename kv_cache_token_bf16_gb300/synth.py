@@ -49,14 +49,17 @@ def rng(seed: int) -> np.random.Generator:
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bf16 (round-to-nearest-even); return the bits.
 
-    NaN maps to the canonical quiet NaN 0x7FC0 (sign kept).
+    NaN maps to the canonical quiet NaN 0x7FC0 (sign kept). For every other
+    value the 32-bit sum below cannot wrap (the largest finite magnitude plus
+    the rounding bias stays below 2^32).
     """
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    lsb = (b >> np.uint64(16)) & np.uint64(1)
-    rounded = ((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
-    nan = np.isnan(np.asarray(x, dtype=np.float32))
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    b = x.view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    rounded = ((b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
     if nan.any():
-        sign = ((b >> np.uint64(16)) & np.uint64(0x8000)).astype(np.uint16)
+        sign = ((b >> np.uint32(16)) & np.uint32(0x8000)).astype(np.uint16)
         rounded = np.where(nan, sign | np.uint16(0x7FC0), rounded)
     return rounded
 
@@ -193,13 +196,24 @@ def long_context_directions(n_kv_heads: int = 8, seed: int | None = None) -> np.
 
 
 def long_context_block(block: int, batch: int = 4, n_kv_heads: int = 8, block_len: int = 8192,
-                       drift: float = 2.0, seed: int | None = None):
-    """Block ``block`` of the 131072-token stream: (K, V) bf16 bits [B, H, block_len, 128]."""
+                       drift: float = 2.0, seed: int | None = None, first_row: int = 0):
+    """Block ``block`` of the 131072-token stream: (K, V) bf16 bits [B, H, block_len, 128].
+
+    Rows ``first_row .. first_row + batch - 1`` of a global batch: every batch
+    row is drawn from its own stream (seeded by the block and the global row),
+    so a batch split into shards draws exactly the rows of the whole batch.
+    """
     u = long_context_directions(n_kv_heads)
-    g = rng(seed_for(5, block) if seed is None else seed)
-    k = g.standard_normal((batch, n_kv_heads, block_len, HEAD_DIM)) + drift * u[None, :, None, :]
-    v = g.standard_normal((batch, n_kv_heads, block_len, HEAD_DIM))
-    return f32_to_bf16_bits(k.astype(np.float32)), f32_to_bf16_bits(v.astype(np.float32))
+    base = seed_for(5, block) if seed is None else seed
+    k = np.empty((batch, n_kv_heads, block_len, HEAD_DIM), np.uint16)
+    v = np.empty_like(k)
+    for j in range(batch):
+        g = np.random.Generator(np.random.PCG64([base, first_row + j]))
+        kr = g.standard_normal((n_kv_heads, block_len, HEAD_DIM), dtype=np.float32)
+        kr += (drift * u[:, None, :]).astype(np.float32)
+        k[j] = f32_to_bf16_bits(kr)
+        v[j] = f32_to_bf16_bits(g.standard_normal((n_kv_heads, block_len, HEAD_DIM), dtype=np.float32))
+    return k, v
 
 
 def long_context_queries(n_heads: int = 8, n_samples: int = 3000, seed: int | None = None):
