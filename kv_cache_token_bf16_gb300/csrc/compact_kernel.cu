@@ -37,10 +37,14 @@ namespace {
 // ---------------------------------------------------------------------------
 constexpr int kCompactThreads = 256;
 
-// Bounded wait on the chunk's copy barrier; raises the device error on timeout.
+// Bounded wait on the chunk's copy barrier (the thread sleeps between polls; 2 s at most);
+// raises the device error on timeout.
 __device__ __forceinline__ bool compact_wait(uint64_t* bar, int* err) {
-  for (int spin = 0; spin < (1 << 22); ++spin)
-    if (tc::mbar_try_wait(bar, 0)) return true;
+  if (tc::mbar_try_wait(bar, 0)) return true;
+  const uint64_t t0 = tc::global_ns();
+  do {
+    if (tc::mbar_try_wait_sleep(bar, 0, 20000)) return true;
+  } while (tc::global_ns() - t0 < 2000000000ull);
   raise_device_error(err, kDevWaitTimeout);
   return false;
 }

@@ -68,7 +68,8 @@ namespace {
 constexpr int kTile = 128;                  // rows of a query or key tile
 constexpr int kTileBytes = kTile * kHeadDim * 2;
 constexpr int kEigThreads = 128;
-constexpr int kMbarSpin = 1 << 22;          // bounded MMA wait (well above a tile's time)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bound of every pipeline wait (2 s, far above a tile's time)
+constexpr uint32_t kWaitSleepNs = 20000;             // longest hardware sleep per poll
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Static split of the attention passes' key tiles over a persistent grid.
@@ -236,12 +237,17 @@ struct UnitCursor {
   }
 };
 
-// Bounded wait on an mbarrier phase. Gives up early once the CTA's failure
-// flag is set; after kMbarSpin polls it sets the flag and the error word.
+// Bounded wait on an mbarrier phase. The waiting thread sleeps in hardware
+// between polls (no issue slots spent while it waits); it gives up early once
+// the CTA's failure flag is set, and after kWaitLimitNs it sets the flag and
+// the error word.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* fail, int* err) {
-  for (int spin = 0; spin < kMbarSpin; ++spin) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    if ((spin & 63) == 63 && *fail) return false;
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::global_ns();
+  for (;;) {
+    if (tc::mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (*fail) return false;
+    if (tc::global_ns() - t0 > kWaitLimitNs) break;
   }
   *fail = 1;
   raise_device_error(err, kDevWaitTimeout);
@@ -250,8 +256,12 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 // The same wait ignoring the failure flag: used to let copies and MMAs already
 // issued finish before the CTA releases its shared and tensor memory.
 __device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity, int* err) {
-  for (int spin = 0; spin < kMbarSpin; ++spin)
-    if (tc::mbar_try_wait(bar, parity)) return;
+  if (tc::mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = tc::global_ns();
+  for (;;) {
+    if (tc::mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return;
+    if (tc::global_ns() - t0 > kWaitLimitNs) break;
+  }
   raise_device_error(err, kDevWaitTimeout);
 }
 
@@ -262,10 +272,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // Shared state of one attention CTA (static shared memory).
+constexpr int kPartSlots = 4;                     // pass 2: ring of key tiles' partial column sums
 struct AttnBars {
   uint64_t stage_full[kLseStages], stage_empty[kLseStages];
   uint64_t fixed_full, fixed_empty;
   uint64_t acc_full[kQuad], acc_empty[kQuad];
+  uint64_t part_full[kPartSlots], part_empty[kPartSlots];
   uint32_t tmem_base;
   int fail;
 };
@@ -385,6 +397,10 @@ __device__ __forceinline__ void attn_setup(AttnBars& b) {
       tc::mbar_init(&b.acc_full[a], 1);
       tc::mbar_init(&b.acc_empty[a], 4);         // the four warps reading accumulator a
     }
+    for (int i = 0; i < kPartSlots; ++i) {
+      tc::mbar_init(&b.part_full[i], 4 * (kQuad - 1));   // the warps of accumulators 0 .. 2
+      tc::mbar_init(&b.part_empty[i], 4);                // the warps of the last accumulator
+    }
     b.fail = 0;
   }
   if (warp == 0) tc::tmem_alloc(&b.tmem_base, kQuad * kTile);
@@ -458,28 +474,48 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_lse_kernel(const __
               if (i < 0 || i > p.k + t) v[c] = -INFINITY;
             }
           }
-          float mx[22];
-#pragma unroll
-          for (int c = 0; c < 21; ++c) mx[c] = fmax3(v[3 * c], v[3 * c + 1], v[3 * c + 2]);
-          mx[21] = v[63];
-#pragma unroll
-          for (int c = 0; c < 7; ++c) mx[c] = fmax3(mx[3 * c], mx[3 * c + 1], mx[3 * c + 2]);
-          mx[7] = mx[21];
-          const float m8 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-          if (m8 > -INFINITY) {
-            const float nm = fmaxf(run_max, m8 * p.scale2);
-            // eight running sums (element c into sum c & 7), two per packed register
+          // Sum of 2^(x - ref) over the half, x = scale2 * logit: eight running sums (element c
+          // into sum c & 7), two per packed register.
+          auto half_sum = [&](float ref) {
             uint64_t sm2[4] = {0ull, 0ull, 0ull, 0ull};
-            const uint64_t sc2 = pack_f32x2(p.scale2, p.scale2), nm2 = pack_f32x2(-nm, -nm);
+            const uint64_t sc2 = pack_f32x2(p.scale2, p.scale2), nr2 = pack_f32x2(-ref, -ref);
 #pragma unroll
             for (int c = 0; c < 64; c += 2)
-              sm2[(c & 7) >> 1] = add_f32x2(sm2[(c & 7) >> 1], ex2_f32x2(fma_f32x2(pack_f32x2(v[c], v[c + 1]), sc2, nm2)));
+              sm2[(c & 7) >> 1] = add_f32x2(sm2[(c & 7) >> 1], ex2_f32x2(fma_f32x2(pack_f32x2(v[c], v[c + 1]), sc2, nr2)));
             float sm[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) split_f32x2(sm2[j], sm[2 * j], sm[2 * j + 1]);
-            const float tot = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-            run_sum = run_sum * ex2(run_max - nm) + tot;         // ex2(-inf) = 0 on the first visible tile
-            run_max = nm;
+            return ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+          };
+          // The reference is the exact maximum of the query's first visible half. Later halves
+          // are summed against it without a maximum of their own while the half's sum stays
+          // below 2^64 (no term can then overflow, and terms far below it are negligible next
+          // to the reference's own term, 1); otherwise (a much larger logit, +inf, NaN) the
+          // half takes its exact maximum and the running sum is rescaled, as lse2 = ref +
+          // log2(sum) holds for any reference.
+          bool exact = true;
+          if (run_max > -INFINITY) {
+            const float tot = half_sum(run_max);
+            if (tot < 0x1p64f) {
+              run_sum += tot;
+              exact = false;
+            }
+          }
+          if (exact) {
+            float mx[22];
+#pragma unroll
+            for (int c = 0; c < 21; ++c) mx[c] = fmax3(v[3 * c], v[3 * c + 1], v[3 * c + 2]);
+            mx[21] = v[63];
+#pragma unroll
+            for (int c = 0; c < 7; ++c) mx[c] = fmax3(mx[3 * c], mx[3 * c + 1], mx[3 * c + 2]);
+            mx[7] = mx[21];
+            const float m8 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            if (m8 > -INFINITY) {
+              const float nm = fmaxf(run_max, m8 * p.scale2);
+              const float tot = half_sum(nm);
+              run_sum = run_sum * ex2(run_max - nm) + tot;         // ex2(-inf) = 0 on the first visible half
+              run_max = nm;
+            }
           }
         }
       }
@@ -521,14 +557,16 @@ __global__ void __launch_bounds__(256) curdkv_lse_merge_kernel(const __grid_cons
 // Pass 2: for each key i and query quad q,
 //   part_q[i] = sum over the quad's queries t with i <= k + t of 2^(x - lse2[t]).
 // Accumulator a holds keys x query tile a; the four warps of one TMEM lane
-// quarter each sum one query tile and combine their sums in shared memory
-// in a fixed order. With one quad the sums are the column sums themselves.
-// ---------------------------------------------------------------------------
+// quarter each sum one query tile. The warps of accumulators 0-2 leave their
+// sums in a four-slot shared-memory ring and the warps of accumulator 3 (the
+// last one the MMAs fill for a key tile) add them in a fixed order and write
+// the result, so the accumulators never wait for each other within a unit.
+// With one quad the sums are the column sums themselves.
 __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const __grid_constant__ CurdkvParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ AttnBars b;
   __shared__ __align__(16) float s_lse[2][kQuad * kTile];
-  __shared__ float s_part[2][kQuad][kTile];
+  __shared__ float s_part[kPartSlots][kQuad - 1][kTile];
   const AttnSched& s = p.sched2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -609,12 +647,21 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
         split_f32x2(s23, sm[2], sm[3]);
         part = (sm[0] + sm[1]) + (sm[2] + sm[3]);
       }
-      s_part[j & 1][a][row] = part;
-      tc::named_sync(1, kSoftWarps * 32);
-      if (a == 0 && !b.fail && i >= 0 && i < p.n) {
-        const float* sp = &s_part[j & 1][0][row];
-        p.colpart[((size_t)u.q * s.bh_count + u.bh) * p.rows + i] =
-            (sp[0] + sp[kTile]) + (sp[2 * kTile] + sp[3 * kTile]);
+      const int slot = j % kPartSlots, round = j / kPartSlots;
+      if (a < kQuad - 1) {
+        // the slot was last used four key tiles ago: wait until the last accumulator read it
+        if (round == 0 || wait_phase(&b.part_empty[slot], (uint32_t)((round - 1) & 1), &b.fail, p.err))
+          s_part[slot][a][row] = part;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&b.part_full[slot]);
+      } else {
+        if (wait_phase(&b.part_full[slot], (uint32_t)(round & 1), &b.fail, p.err) && !b.fail && i >= 0 &&
+            i < p.n) {
+          const float* sp = &s_part[slot][0][row];
+          p.colpart[((size_t)u.q * s.bh_count + u.bh) * p.rows + i] = (sp[0] + sp[kTile]) + (sp[2 * kTile] + part);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&b.part_empty[slot]);
       }
       u.next(s, p.m);
     }

@@ -170,10 +170,14 @@ constexpr int kE1StageBytes = 32768;     // one chunk of K rows and the same row
 constexpr int kE1PsChunk = 1024;         // positions / scores moved per shared-memory round
 constexpr int kE1Smem = kE1Stages * kE1StageBytes;
 
-// Bounded wait on a bulk-copy barrier; raises the device error on timeout.
+// Bounded wait on a bulk-copy barrier (the thread sleeps between polls; 2 s at most); raises
+// the device error on timeout.
 __device__ __forceinline__ bool e1_wait(uint64_t* bar, uint32_t parity, int* err) {
-  for (int spin = 0; spin < (1 << 22); ++spin)
-    if (tc::mbar_try_wait(bar, parity)) return true;
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::global_ns();
+  do {
+    if (tc::mbar_try_wait_sleep(bar, parity, 20000)) return true;
+  } while (tc::global_ns() - t0 < 2000000000ull);
   raise_device_error(err, kDevWaitTimeout);
   return false;
 }
