@@ -164,12 +164,18 @@ __device__ __forceinline__ uint64_t ex2_f32x2(uint64_t x) {
 }
 
 // 8 MMAs (K = 128 in steps of 16): D[128 x 128] = A[128 x 128] * B[128 x 128]^T.
+// The steps' descriptors differ from the tile's only in the start-address field
+// (bits 0-13, byte address / 16): a step adds its offset / 16 to the low word;
+// tiles lie below 256 KB of shared memory, so the field never carries over.
 __device__ __forceinline__ void issue_tile_mma(uint32_t tmem, uint32_t a, uint32_t b) {
   constexpr uint32_t idesc = tc::idesc_bf16_f32(kTile, kTile);
+  const uint64_t da = tc::sw128_desc(a), db = tc::sw128_desc(b);
+  const uint32_t a_lo = (uint32_t)da, b_lo = (uint32_t)db, a_hi = (uint32_t)(da >> 32), b_hi = (uint32_t)(db >> 32);
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    const uint32_t off = (uint32_t)((s >> 2) * kTile * 128 + (s & 3) * 32);
-    tc::mma_bf16(tmem, tc::sw128_desc(a + off), tc::sw128_desc(b + off), idesc, s > 0 ? 1u : 0u);
+    const uint32_t off16 = (uint32_t)(((s >> 2) * kTile * 128 + (s & 3) * 32) >> 4);
+    tc::mma_bf16(tmem, ((uint64_t)a_hi << 32) | (uint64_t)(a_lo + off16), ((uint64_t)b_hi << 32) | (uint64_t)(b_lo + off16),
+                 idesc, s > 0 ? 1u : 0u);
   }
 }
 
@@ -369,17 +375,18 @@ __device__ __forceinline__ bool warp_wait_acc(uint64_t* bar, uint32_t parity, At
   return __all_sync(0xffffffffu, ok);
 }
 
-// 64 accumulator columns of this thread's row (two 32-column loads, one wait).
+// 64 accumulator columns of this thread's row: one load and its wait in one asm statement, so
+// no use of the registers can be scheduled before the data is there.
 __device__ __forceinline__ void load64(uint32_t taddr, float (&v)[64]) {
-  uint32_t r0[32], r1[32];
-  tc::tmem_ld32_nowait(taddr, r0);
-  tc::tmem_ld32_nowait(taddr + 32, r1);
-  tc::tmem_wait_ld32x2(r0, r1);
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    v[c] = __uint_as_float(r0[c]);
-    v[c + 32] = __uint_as_float(r1[c]);
-  }
+  for (int c = 0; c < 64; ++c) v[c] = __uint_as_float(r[c]);
 }
 
 // Setup shared by both passes: barriers, TMEM, this CTA's share of the tiles.

@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __gr
   }
   uint32_t dest = block_excl_sum<kThreads>((uint32_t)__popc(keep_bits), scan, &total);
   int32_t* src_map = L.src_map + (size_t)bh * s.cap;
+  const int chunk_shift = __ffs(s.chunk) - 1;         // compaction chunks are 32 or 64 rows: a power of two
   int first_drop = s.k;
   uint32_t old_kept = 0u;
   // wait ranges: the thread's rows and destinations both increase, so each source chunk's
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __gr
       else raise_device_error(P.err, kDevBadIndex);
       if (i < s.k) {
         ++old_kept;
-        const int cd = (int)dest / s.chunk, cs = i / s.chunk;
+        const int cd = (int)dest >> chunk_shift, cs = i >> chunk_shift;
         if (cd < cs) {
           if (cs != run_cs) {
             if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
@@ -248,7 +249,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __gr
     }
   }
   if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
-  if (first_drop < s.k) atomicMin(&s_first, first_drop);
+  // the first dropped kept row: one shared atomic per warp (a per-thread atomic on one address
+  // serialises hundreds of updates)
+  const int wfirst = __reduce_min_sync(0xffffffffu, first_drop);
+  if (lane == 0 && wfirst < s.k) atomicMin(&s_first, wfirst);
   const uint32_t wsum = __reduce_add_sync(0xffffffffu, old_kept);
   if (lane == 0 && wsum) atomicAdd(&s_old_kept, (int)wsum);
   __syncthreads();
@@ -371,6 +375,7 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
   }
   uint32_t dest = block_excl_sum<kThreads>(keep_count, scan, &total);
   int32_t* src_map = L.src_map + (size_t)bh * s.cap;
+  const int chunk_shift = __ffs(s.chunk) - 1;         // compaction chunks are 32 or 64 rows: a power of two
   int first_drop = s.k;
   uint32_t old_kept = 0u;
   {
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
         else raise_device_error(P.err, kDevBadIndex);
         if (i < s.k) {
           ++old_kept;
-          const int cd = (int)dest / s.chunk, cs = i / s.chunk;
+          const int cd = (int)dest >> chunk_shift, cs = i >> chunk_shift;
           if (cd < cs) {
             if (cs != run_cs) {
               if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
@@ -403,7 +408,10 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
     }
     if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
   }
-  if (first_drop < s.k) atomicMin(&s_first, first_drop);
+  // the first dropped kept row: one shared atomic per warp (a per-thread atomic on one address
+  // serialises hundreds of updates)
+  const int wfirst = __reduce_min_sync(0xffffffffu, first_drop);
+  if (lane == 0 && wfirst < s.k) atomicMin(&s_first, wfirst);
   const uint32_t wsum = __reduce_add_sync(0xffffffffu, old_kept);
   if (lane == 0 && wsum) atomicAdd(&s_old_kept, (int)wsum);
   __syncthreads();
