@@ -20,6 +20,12 @@ enum DeviceError : int {
 // Spin limit of every inter-CTA wait (each spin sleeps ~100 ns; ~0.4 s total).
 constexpr int kSpinLimit = 1 << 22;
 
+// Programmatic dependent launch: every kernel of the eviction path is launched
+// so that it may start while the previous kernel in the stream finishes, and
+// waits here, before touching any memory, until that kernel has completed and
+// its writes are visible. Without the launch attribute this is a no-op.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void raise_device_error(int* err, int code) {
   atomicCAS(err, 0, code);
 }

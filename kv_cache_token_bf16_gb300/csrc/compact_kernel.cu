@@ -51,6 +51,7 @@ __device__ __forceinline__ bool compact_wait(uint64_t* bar, int* err) {
 
 template <int kRowBytes, int kChunk>
 __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_constant__ GroupParams P) {
+  pdl_wait();
   static_assert(kChunk <= kCompactThreads, "one thread per destination row");
   extern __shared__ __align__(128) unsigned char c_smem[];   // the chunk's K rows, then its V rows
   __shared__ uint64_t s_bar;
@@ -175,8 +176,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
 
 template <typename Kernel>
 cudaError_t launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const GroupParams& P) {
-  kernel<<<grid, block, smem, st>>>(P);
-  return cudaGetLastError();
+  return launch_pdl(kernel, grid, block, smem, st, nullptr, P);
 }
 
 }  // namespace

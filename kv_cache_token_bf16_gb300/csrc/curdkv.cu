@@ -429,6 +429,7 @@ __device__ __forceinline__ void attn_teardown(AttnBars& b) {
 // several CTAs leaves one partial per CTA (slot = CTA - first CTA of the unit).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_lse_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ AttnBars b;
   const AttnSched& s = p.sched1;
@@ -543,6 +544,7 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_lse_kernel(const __
 
 // Merge the per-CTA partials: lse2[t] = log2 sum_s s_s 2^(m_s). grid = (ceil(m / 256), B*H).
 __global__ void __launch_bounds__(256) curdkv_lse_merge_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   const AttnSched& s = p.sched1;
   const int bh = blockIdx.y, t = blockIdx.x * 256 + threadIdx.x;
   if (t >= p.m) return;
@@ -570,6 +572,7 @@ __global__ void __launch_bounds__(256) curdkv_lse_merge_kernel(const __grid_cons
 // the result, so the accumulators never wait for each other within a unit.
 // With one quad the sums are the column sums themselves.
 __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ AttnBars b;
   __shared__ __align__(16) float s_lse[2][kQuad * kTile];
@@ -680,6 +683,7 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
 // tiles include row i. grid = (ceil(n / 256), B*H); only launched with two
 // or more quads.
 __global__ void __launch_bounds__(256) curdkv_colsum_merge_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   const AttnSched& s = p.sched2;
   const int bh = blockIdx.y, i = blockIdx.x * 256 + threadIdx.x;
   if (i >= p.n) return;
@@ -697,6 +701,7 @@ __global__ void __launch_bounds__(256) curdkv_colsum_merge_kernel(const __grid_c
 // from theirs (their own query already left out by the column-sum pass).
 // grid = (ceil(n / 256), B*H).
 __global__ void __launch_bounds__(256) h2o_mass_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   const int bh = blockIdx.y, i = blockIdx.x * 256 + threadIdx.x;
   if (i >= p.n) return;
   const float a = p.attn[(size_t)bh * p.rows + i];
@@ -737,6 +742,7 @@ __host__ __device__ constexpr bool small_attn_fits(int m, int n) {
 
 template <int kM>
 __global__ void __launch_bounds__(kSmallAttnThreads) curdkv_attn_small_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   static_assert(kM >= 1 && kM <= kSmallAttnMaxM, "queries per CTA");
   extern __shared__ __align__(16) float s_term[];            // [m][n]: logits, then 2^(l - max)
   __shared__ float s_red[kSmallAttnWarps][kSmallAttnMaxM];
@@ -890,6 +896,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
 }
 
 __global__ void __launch_bounds__(kGramThreads, 1) curdkv_gram_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ GramBars b;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1199,6 +1206,7 @@ struct EigHalves {
 template <int kR>
 __global__ void __launch_bounds__(kEigThreads, kR <= 16 ? 2 : 1)
     curdkv_eig_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   extern __shared__ __align__(16) unsigned char eig_raw[];
   EigSmem<kR>& s = *reinterpret_cast<EigSmem<kR>*>(eig_raw);
   const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1747,6 +1755,7 @@ struct LevBars {
 };
 
 __global__ void __launch_bounds__(kLevThreads, 1) curdkv_leverage_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ LevBars b;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1905,6 +1914,7 @@ __global__ void __launch_bounds__(kLevThreads, 1) curdkv_leverage_kernel(const _
 
 // Append the block (cache stays within budget): grid = (ceil(m / 64), B*H), block = 256.
 __global__ void __launch_bounds__(256) curdkv_append_kernel(const __grid_constant__ CurdkvParams p) {
+  pdl_wait();
   const int bh = blockIdx.y, b = bh / p.heads;
   const int c = threadIdx.x & 15, hw = threadIdx.x >> 4;
   constexpr int kRowBytes = kHeadDim * 2;
@@ -2090,83 +2100,70 @@ int curdkv_update(evict_handle* h, const void* k, const void* v, const int32_t* 
     e = timed_launch(h, kKidCurdkvAttnSmall, [&] {
       const size_t smem = (size_t)m * n * sizeof(float);
       if (m == 1)
-        curdkv_attn_small_kernel<1><<<bh, kSmallAttnThreads, smem, sm>>>(p);
+        return launch_pdl(curdkv_attn_small_kernel<1>, dim3(bh), dim3(kSmallAttnThreads), smem, sm, nullptr, p);
       else if (m == 2)
-        curdkv_attn_small_kernel<2><<<bh, kSmallAttnThreads, smem, sm>>>(p);
+        return launch_pdl(curdkv_attn_small_kernel<2>, dim3(bh), dim3(kSmallAttnThreads), smem, sm, nullptr, p);
       else if (m <= 4)
-        curdkv_attn_small_kernel<4><<<bh, kSmallAttnThreads, smem, sm>>>(p);
+        return launch_pdl(curdkv_attn_small_kernel<4>, dim3(bh), dim3(kSmallAttnThreads), smem, sm, nullptr, p);
       else
-        curdkv_attn_small_kernel<8><<<bh, kSmallAttnThreads, smem, sm>>>(p);
-      return cudaGetLastError();
+        return launch_pdl(curdkv_attn_small_kernel<8>, dim3(bh), dim3(kSmallAttnThreads), smem, sm, nullptr, p);
     });
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV short-block attention launch");
   } else {
   e = timed_launch(h, kKidCurdkvLse, [&] {
-    curdkv_lse_kernel<<<p.sched1.ctas, kAttnCtaThreads, attn_smem_bytes(kLseStages), sm>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(curdkv_lse_kernel, dim3(p.sched1.ctas), dim3(kAttnCtaThreads), attn_smem_bytes(kLseStages), sm,
+                      nullptr, p);
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention pass 1 launch");
   e = timed_launch(h, kKidCurdkvLseMerge, [&] {
-    curdkv_lse_merge_kernel<<<dim3((m + 255) / 256, bh), 256, 0, sm>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(curdkv_lse_merge_kernel, dim3((m + 255) / 256, bh), dim3(256), 0, sm, nullptr, p);
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention merge launch");
   e = timed_launch(h, kKidCurdkvColsum, [&] {
-    curdkv_colsum_kernel<<<p.sched2.ctas, kAttnCtaThreads, attn_smem_bytes(kColStages), sm>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(curdkv_colsum_kernel, dim3(p.sched2.ctas), dim3(kAttnCtaThreads), attn_smem_bytes(kColStages),
+                      sm, nullptr, p);
   });
   if (e != cudaSuccess) return cuda_fail(e, "CurDKV attention pass 2 launch");
   if (p.sched2.Q > 1) {
     e = timed_launch(h, kKidCurdkvColsumMerge, [&] {
-      curdkv_colsum_merge_kernel<<<dim3((n + 255) / 256, bh), 256, 0, sm>>>(p);
-      return cudaGetLastError();
+      return launch_pdl(curdkv_colsum_merge_kernel, dim3((n + 255) / 256, bh), dim3(256), 0, sm, nullptr, p);
     });
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV column-sum merge launch");
   }
   if (p.self_excluded) {
     e = timed_launch(h, kKidH2oMass, [&] {
-      h2o_mass_kernel<<<dim3((n + 255) / 256, bh), 256, 0, sm>>>(p);
-      return cudaGetLastError();
+      return launch_pdl(h2o_mass_kernel, dim3((n + 255) / 256, bh), dim3(256), 0, sm, nullptr, p);
     });
     if (e != cudaSuccess) return cuda_fail(e, "H2O mass launch");
   }
   }
   if (!p.self_excluded) {
     e = timed_launch(h, kKidCurdkvGram, [&] {
-      cudaLaunchConfig_t lc = {};
-      lc.gridDim = dim3(p.gram_cluster * bh);
-      lc.blockDim = dim3(kGramThreads);
-      lc.dynamicSmemBytes = kGramSmem;
-      lc.stream = sm;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = (unsigned)p.gram_cluster;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      lc.attrs = attr;
-      lc.numAttrs = 1;
-      return cudaLaunchKernelEx(&lc, curdkv_gram_kernel, p);
+      cudaLaunchAttribute cluster;
+      cluster.id = cudaLaunchAttributeClusterDimension;
+      cluster.val.clusterDim.x = (unsigned)p.gram_cluster;
+      cluster.val.clusterDim.y = 1;
+      cluster.val.clusterDim.z = 1;
+      return launch_pdl(curdkv_gram_kernel, dim3(p.gram_cluster * bh), dim3(kGramThreads), kGramSmem, sm, &cluster, p);
     });
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV Gram launch");
     e = timed_launch(h, kKidCurdkvEig, [&] {
       if (p.rank <= 16)
-        curdkv_eig_kernel<16><<<bh, kEigThreads, sizeof(EigSmem<16>), sm>>>(p);
-      else
-        curdkv_eig_kernel<kCurdkvMaxRank><<<bh, kEigThreads, sizeof(EigSmem<kCurdkvMaxRank>), sm>>>(p);
-      return cudaGetLastError();
+        return launch_pdl(curdkv_eig_kernel<16>, dim3(bh), dim3(kEigThreads), sizeof(EigSmem<16>), sm, nullptr, p);
+      return launch_pdl(curdkv_eig_kernel<kCurdkvMaxRank>, dim3(bh), dim3(kEigThreads), sizeof(EigSmem<kCurdkvMaxRank>),
+                        sm, nullptr, p);
     });
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV eigensolver launch");
     e = timed_launch(h, kKidCurdkvLeverage, [&] {
       const long long items = (long long)bh * ((p.k + kTile - 1) / kTile + (m + kTile - 1) / kTile);
-      curdkv_leverage_kernel<<<(int)std::min<long long>(st.sm_count, items), kLevThreads, kLevSmem, sm>>>(p);
-      return cudaGetLastError();
+      return launch_pdl(curdkv_leverage_kernel, dim3((int)std::min<long long>(st.sm_count, items)), dim3(kLevThreads),
+                        kLevSmem, sm, nullptr, p);
     });
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV leverage launch");
   }
   if (n <= c.budget) {
     e = timed_launch(h, kKidAppend, [&] {
-      curdkv_append_kernel<<<dim3((m + 63) / 64, bh), 256, 0, sm>>>(p);
-      return cudaGetLastError();
+      return launch_pdl(curdkv_append_kernel, dim3((m + 63) / 64, bh), dim3(256), 0, sm, nullptr, p);
     });
     if (e != cudaSuccess) return cuda_fail(e, "CurDKV append launch");
     h->n_kept = n;

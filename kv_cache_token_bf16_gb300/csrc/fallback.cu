@@ -110,6 +110,7 @@ __device__ __forceinline__ float trace128(const float* m, int ld, float* red) {
 // grid = units * cluster (cluster dims (cluster, 1, 1)), block = 256, dynamic shared memory kFzSmem.
 template <bool kBf16>
 __global__ void __launch_bounds__(kFzThreads) freeze_kernel(const __grid_constant__ GroupParams P) {
+  pdl_wait();
   extern __shared__ __align__(16) float fz_smem[];
   float* C = fz_smem;                            // padded: the unit's centred Gram (rank 0: the sum)
   float* S1 = fz_smem + kFzPadded;               // key tile, then the squarings (dense, the last padded)
@@ -355,20 +356,14 @@ cudaError_t launch_freeze(const GroupParams& P, int dtype_bytes, cudaStream_t st
   if (e != cudaSuccess) return e;
   const int n = P.s.k + P.s.m;
   int cl = std::max(1, std::min({kFzMaxCluster, sms / units, n / kFzMinSliceRows}));
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3((unsigned)(units * cl));
-  lc.blockDim = dim3(kFzThreads);
-  lc.dynamicSmemBytes = kFzSmem;
-  lc.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  if (dtype_bytes == 2) return cudaLaunchKernelEx(&lc, freeze_kernel<true>, P);
-  return cudaLaunchKernelEx(&lc, freeze_kernel<false>, P);
+  cudaLaunchAttribute cluster;
+  cluster.id = cudaLaunchAttributeClusterDimension;
+  cluster.val.clusterDim.x = (unsigned)cl;
+  cluster.val.clusterDim.y = 1;
+  cluster.val.clusterDim.z = 1;
+  const dim3 grid((unsigned)(units * cl)), block(kFzThreads);
+  if (dtype_bytes == 2) return launch_pdl(freeze_kernel<true>, grid, block, kFzSmem, st, &cluster, P);
+  return launch_pdl(freeze_kernel<false>, grid, block, kFzSmem, st, &cluster, P);
 }
 
 }  // namespace evict

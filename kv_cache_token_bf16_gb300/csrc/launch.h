@@ -3,9 +3,33 @@
 
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "params.h"
 
 namespace evict {
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel in the stream is still finishing (it waits for it
+// in its first statement, pdl_wait), which hides the launch gap between the
+// path's kernels. `extra` may add one more attribute (a cluster shape).
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       const cudaLaunchAttribute* extra, Args&&... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (extra) attr[n++] = *extra;
+  lc.attrs = attr;
+  lc.numAttrs = n;
+  return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+}
 
 // Rows per compaction chunk for an element size of 2 (bf16) or 4 (fp32) bytes.
 int compact_chunk_rows(int dtype_bytes);

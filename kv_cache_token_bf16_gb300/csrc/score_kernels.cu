@@ -27,6 +27,7 @@ constexpr int kScoreRowsPerCta = (kScoreThreads / 16) * kRowsPerHalfWarp;   // 6
 // ---------------------------------------------------------------------------
 template <bool kBf16, int kMethod>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(const __grid_constant__ GroupParams P) {
+  pdl_wait();
   const Shape& s = P.s;
   const int bhn = s.batch * s.heads;
   const int u = blockIdx.y;
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const __grid_const
 // ---------------------------------------------------------------------------
 template <bool kBf16, int kMethod>
 __global__ void __launch_bounds__(kScoreThreads) append_kernel(const __grid_constant__ GroupParams P) {
+  pdl_wait();
   const Shape& s = P.s;
   const int bhn = s.batch * s.heads;
   const int u = blockIdx.y;
@@ -113,8 +115,7 @@ __global__ void __launch_bounds__(kScoreThreads) append_kernel(const __grid_cons
 
 template <typename Kernel>
 cudaError_t launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const GroupParams& P) {
-  kernel<<<grid, block, smem, st>>>(P);
-  return cudaGetLastError();
+  return launch_pdl(kernel, grid, block, smem, st, nullptr, P);
 }
 
 }  // namespace
@@ -184,6 +185,7 @@ __device__ __forceinline__ bool e1_wait(uint64_t* bar, uint32_t parity, int* err
 
 template <bool kBf16, int kMethod>
 __global__ void __launch_bounds__(kE1Threads, 2) evict1_kernel(const __grid_constant__ GroupParams P) {
+  pdl_wait();
   extern __shared__ __align__(128) unsigned char e1_smem[];   // kE1Stages x (K chunk, V chunk)
   __shared__ float s_new[kE1MaxBlock];
   __shared__ unsigned long long s_best[kE1Warps];

@@ -86,6 +86,7 @@ __device__ __forceinline__ void store_waits(const int* wlo, const int* whi, int2
 
 template <int kThreads, int kPer, int kMinBlocks = 1>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __grid_constant__ GroupParams P) {
+  pdl_wait();
   __shared__ uint32_t hist[kBins];
   __shared__ uint32_t scan[65];
   __shared__ uint32_t s_min[32], s_max[32];
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __gr
 // ---------------------------------------------------------------------------
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_constant__ GroupParams P) {
+  pdl_wait();
   extern __shared__ uint32_t keys[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t scan[65];
@@ -421,8 +423,7 @@ __global__ void __launch_bounds__(kThreads) select_smem_kernel(const __grid_cons
 
 template <typename Kernel>
 cudaError_t launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const GroupParams& P) {
-  kernel<<<grid, block, smem, st>>>(P);
-  return cudaGetLastError();
+  return launch_pdl(kernel, grid, block, smem, st, nullptr, P);
 }
 
 }  // namespace
