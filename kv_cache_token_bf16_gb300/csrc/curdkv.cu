@@ -193,16 +193,17 @@ __device__ __forceinline__ void issue_tile_mma(uint32_t tmem, uint32_t a, uint32
 // takes an equal contiguous share: one wave of CTAs with equal work; a unit
 // may be shared by neighbouring CTAs (pass 1 then leaves one partial per CTA).
 //
-// Roles (576 threads): warps 0-15 read the accumulators (warp w: TMEM lanes
+// Roles (608 threads): warps 0-15 read the accumulators (warp w: TMEM lanes
 // 32 (w % 4) .. +31, accumulator w / 4 = query tile w / 4 of the quad);
-// warp 16 issues the TMA loads; warp 17 issues the MMAs. Each query tile has
+// warp 16 issues the TMA loads; warps 17 and 18 issue the MMAs of
+// accumulators {0, 2} and {1, 3}. Each query tile has
 // its own 128-column fp32 accumulator (512 TMEM columns), so the MMAs of one
 // accumulator run while the other three are read. mbarriers connect the
 // roles; every wait is bounded and a timeout stops the CTA cleanly.
 // ---------------------------------------------------------------------------
 constexpr int kQuad = 4;                          // fixed query tiles per unit
 constexpr int kSoftWarps = 16;
-constexpr int kAttnCtaThreads = (kSoftWarps + 2) * 32;
+constexpr int kAttnCtaThreads = (kSoftWarps + 3) * 32;   // + the TMA warp and two MMA warps
 constexpr int kMaxLseSplit = 8;                   // CTAs that may share one unit in pass 1
 constexpr int kLseStages = 3, kColStages = 2;
 constexpr int attn_smem_bytes(int stages) { return (kQuad + stages) * kTileBytes + 1024; }
@@ -330,16 +331,21 @@ __device__ void attn_producer(const CurdkvParams& p, const AttnSched& s, AttnBar
   if (units > 0) drain_phase(&b.fixed_full, (uint32_t)((units - 1) & 1), p.err);
 }
 
+// Two MMA-issuing threads, one for accumulators {0, 2} and one for {1, 3}: the
+// softmax warps hand the accumulators back one after another, and each thread
+// issues its next tile's MMAs as soon as its own accumulators are free, not
+// behind the other pair's. Both release the key stage and the fixed tiles
+// (those barriers count kMmaThreads arrivals).
+constexpr int kMmaThreads = 2;
 template <int kStagesT, bool kColsum>
 __device__ void attn_mma(const CurdkvParams& p, const AttnSched& s, AttnBars& b, uint32_t tmem, uint32_t fixed,
-                         uint32_t stage0, long long g0, long long g1) {
+                         uint32_t stage0, long long g0, long long g1, int first) {
   UnitCursor u;
   u.init(s, p.m, g0);
-  int units = 0, uses[kQuad] = {0, 0, 0, 0};
+  int units = 0, uses[2] = {0, 0};
   bool ok = true;
   for (long long g = g0; g < g1 && ok; ++g) {
     const int j = (int)(g - g0);
-    const int nq = quad_rows(p.m, u.q);
     if (g == g0 || u.kt == 0) {
       if (!wait_phase(&b.fixed_full, (uint32_t)(units & 1), &b.fail, p.err)) break;
       ++units;
@@ -347,17 +353,21 @@ __device__ void attn_mma(const CurdkvParams& p, const AttnSched& s, AttnBars& b,
     const int st = j % kStagesT;
     if (!wait_phase(&b.stage_full[st], (uint32_t)((j / kStagesT) & 1), &b.fail, p.err)) break;
     const uint32_t keys = stage0 + st * kTileBytes;
-    for (int a = 0; a < nq; ++a) {
-      if (!wait_phase(&b.acc_empty[a], (uint32_t)((uses[a] & 1) ^ 1), &b.fail, p.err)) {
+    const int nq = quad_rows(p.m, u.q);
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int a = first + kMmaThreads * x;
+      if (a >= nq) continue;
+      if (!wait_phase(&b.acc_empty[a], (uint32_t)((uses[x] & 1) ^ 1), &b.fail, p.err)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      const uint32_t q_tile = fixed + a * kTileBytes;
-      if (kColsum) issue_tile_mma(tmem + (uint32_t)(a * kTile), keys, q_tile);
-      else issue_tile_mma(tmem + (uint32_t)(a * kTile), q_tile, keys);
+      const uint32_t q_tile = fixed + a * kTileBytes, d = tmem + (uint32_t)(a * kTile);
+      if (kColsum) issue_tile_mma(d, keys, q_tile);
+      else issue_tile_mma(d, q_tile, keys);
       tc::mma_commit(&b.acc_full[a]);
-      ++uses[a];
+      ++uses[x];
     }
     if (!ok) break;
     tc::mma_commit(&b.stage_empty[st]);
@@ -365,8 +375,9 @@ __device__ void attn_mma(const CurdkvParams& p, const AttnSched& s, AttnBars& b,
     u.next(s, p.m);
   }
   // the accumulators' last MMAs must finish before TMEM is released
-  for (int a = 0; a < kQuad; ++a)
-    if (uses[a] > 0) drain_phase(&b.acc_full[a], (uint32_t)((uses[a] - 1) & 1), p.err);
+#pragma unroll
+  for (int x = 0; x < 2; ++x)
+    if (uses[x] > 0) drain_phase(&b.acc_full[first + kMmaThreads * x], (uint32_t)((uses[x] - 1) & 1), p.err);
 }
 
 // Bounded, warp-uniform wait of an accumulator-reading warp.
@@ -396,10 +407,10 @@ __device__ __forceinline__ void attn_setup(AttnBars& b) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesT; ++i) {
       tc::mbar_init(&b.stage_full[i], 1);
-      tc::mbar_init(&b.stage_empty[i], 1);
+      tc::mbar_init(&b.stage_empty[i], 2);         // released by both MMA threads
     }
     tc::mbar_init(&b.fixed_full, 1);
-    tc::mbar_init(&b.fixed_empty, 1);
+    tc::mbar_init(&b.fixed_empty, 2);
     for (int a = 0; a < kQuad; ++a) {
       tc::mbar_init(&b.acc_full[a], 1);
       tc::mbar_init(&b.acc_empty[a], 4);         // the four warps reading accumulator a
@@ -442,8 +453,8 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_lse_kernel(const __
   if (warp == kSoftWarps) {
     if (lane == 0) attn_producer<kLseStages>(p, s, b, fixed, stage0, g0, g1);
     __syncwarp();
-  } else if (warp == kSoftWarps + 1) {
-    if (lane == 0) attn_mma<kLseStages, false>(p, s, b, tmem, fixed, stage0, g0, g1);
+  } else if (warp > kSoftWarps) {
+    if (lane == 0) attn_mma<kLseStages, false>(p, s, b, tmem, fixed, stage0, g0, g1, warp - kSoftWarps - 1);
     __syncwarp();
   } else {
     const int a = warp >> 2, row = 32 * (warp & 3) + lane;
@@ -587,8 +598,8 @@ __global__ void __launch_bounds__(kAttnCtaThreads, 1) curdkv_colsum_kernel(const
   if (warp == kSoftWarps) {
     if (lane == 0) attn_producer<kColStages>(p, s, b, fixed, stage0, g0, g1);
     __syncwarp();
-  } else if (warp == kSoftWarps + 1) {
-    if (lane == 0) attn_mma<kColStages, true>(p, s, b, tmem, fixed, stage0, g0, g1);
+  } else if (warp > kSoftWarps) {
+    if (lane == 0) attn_mma<kColStages, true>(p, s, b, tmem, fixed, stage0, g0, g1, warp - kSoftWarps - 1);
     __syncwarp();
   } else {
     const int a = warp >> 2, row = 32 * (warp & 3) + lane, tid = threadIdx.x;
