@@ -51,15 +51,20 @@ __device__ __forceinline__ uint32_t block_excl_sum(uint32_t x, uint32_t* scratch
 // Protected top-k selection: one CTA per (layer, b, h), keys in registers.
 //
 // Thread t owns the contiguous rows [t*kPer, t*kPer + kPer) and their 32-bit
-// order keys. A block min/max over the unprotected keys gives the bits every
-// candidate shares; the remaining bits are resolved most-significant first
-// in digits of up to 11 bits (a 2048-bin shared histogram per pass, later
-// passes only counting keys that still match the prefix), which yields the
-// key T of the q-th best unprotected row and how many rows equal to T fit.
-// Two block scans then give each segment its count of equal rows and of kept
-// rows before it; each thread writes its survivors' source rows to
-// src_map[destination] in index order. Also zeroes the unit's compaction
-// flags and chunk counter.
+// order keys; bit j of its masks stands for row t*kPer + j. A block min/max
+// over the unprotected keys gives the bits every candidate shares; the
+// remaining bits are resolved most-significant first in digits of up to 11
+// bits: each pass counts the candidates still matching the prefix in a
+// 2048-bin shared histogram, and one warp scans it for the bin holding the
+// rem-th best. Passes stop once every bit is resolved or once the whole bin
+// is admitted (rem equals its count): then every row of the bin is kept and
+// its low bits never decide anything. The result is a masked threshold: rows
+// whose masked key is above the prefix are kept, and of the rows whose masked
+// key equals it, the first eq_quota in index order. One block scan of the
+// per-thread counts of both classes gives each thread its first destination;
+// each thread then writes the source row of each of its survivors to
+// src_map[destination]. Also zeroes the unit's compaction flags and chunk
+// counter.
 // ---------------------------------------------------------------------------
 constexpr int kDigitBits = 11;
 constexpr int kBins = 1 << kDigitBits;
@@ -84,181 +89,254 @@ __device__ __forceinline__ void store_waits(const int* wlo, const int* whi, int2
   for (int c = threadIdx.x; c < chunks; c += blockDim.x) out[c] = make_int2(wlo[c], whi[c]);
 }
 
+// Bits [a, b) of a 32-bit mask (0 <= a, b <= 31).
+__device__ __forceinline__ uint32_t bit_range(int a, int b) {
+  return b > a ? ((1u << (b - a)) - 1u) << a : 0u;
+}
+
+// Inclusive warp sum.
+__device__ __forceinline__ uint32_t warp_incl_sum(uint32_t x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// One warp finds the bin holding the rem-th candidate counted from the top of
+// a 2048-bin histogram: lane l sums the 64 bins of group 31 - l (groups from
+// the top; its 16 vector loads are rotated by l so that no two lanes of a
+// quarter-warp share a bank), a warp scan picks the group, and the group's
+// bins, two per lane from its top, a second scan picks the bin. Returns the
+// bin; *above gets the candidates in higher bins, *count the bin's count.
+__device__ __forceinline__ int warp_find_bin(const uint32_t* h, uint32_t rem, uint32_t* above, uint32_t* count) {
+  const int lane = threadIdx.x & 31;
+  const int g = 31 - lane;                        // this lane's group: bins [64g, 64g + 64)
+  const uint4* gv = reinterpret_cast<const uint4*>(h + 64 * g);
+  uint32_t sum = 0u;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const uint4 v = gv[(c + lane) & 15];
+    sum += (v.x + v.y) + (v.z + v.w);
+  }
+  const uint32_t incl = warp_incl_sum(sum);
+  const unsigned hit = __ballot_sync(0xffffffffu, incl - sum < rem && rem <= incl);
+  const int src = __ffs(hit) - 1;
+  const uint32_t gabove = __shfl_sync(0xffffffffu, incl - sum, src);
+  const int top = 64 * (31 - src) + 63 - 2 * lane;  // this lane's two bins: top, top - 1
+  const uint32_t c0 = h[top], c1 = h[top - 1];
+  const uint32_t pair = c0 + c1;
+  const uint32_t pincl = warp_incl_sum(pair);
+  const uint32_t pexcl = gabove + pincl - pair;
+  const unsigned phit = __ballot_sync(0xffffffffu, pexcl < rem && rem <= pexcl + pair);
+  const int psrc = __ffs(phit) - 1;
+  const bool first = pexcl + c0 >= rem;           // the rem-th lies in the higher bin of the pair
+  const int bin = first ? top : top - 1;
+  const uint32_t bab = first ? pexcl : pexcl + c0;
+  const uint32_t bcnt = first ? c0 : c1;
+  *above = __shfl_sync(0xffffffffu, bab, psrc);
+  *count = __shfl_sync(0xffffffffu, bcnt, psrc);
+  return __shfl_sync(0xffffffffu, bin, psrc);
+}
+
 template <int kThreads, int kPer, int kMinBlocks = 1>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __grid_constant__ GroupParams P) {
+  constexpr int kWarps = kThreads / kWarp;
+  static_assert(kPer < 32, "row masks are 32-bit");
+  static_assert(kThreads * kPer < 65536, "block counts are packed in 16-bit halves");
   pdl_wait();
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t scan[65];
-  __shared__ uint32_t s_min[32], s_max[32];
-  __shared__ uint32_t s_prefix, s_rem;
+  __shared__ __align__(16) uint32_t hist[2][kBins];   // this pass's histogram and the next one's
+  __shared__ uint32_t s_red[2][32];               // per-warp min / max
+  __shared__ uint32_t s_cnt[32];                  // per-warp totals of the admission counts
+  __shared__ uint32_t s_prefix, s_rem, s_nbin;
   __shared__ int s_first, s_old_kept;
-  __shared__ int s_wlo[kMaxWaitChunks], s_whi[kMaxWaitChunks];
+  __shared__ int s_kb[kMaxWaitChunks];            // per source chunk holding kept rows: survivors before it
   const Shape& s = P.s;
   const int bhn = s.batch * s.heads;
   const int u = blockIdx.x;
   const LayerPtrs& L = P.L[u / bhn];
   const int bh = u % bhn;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kWarps = kThreads / 32;
   const int chunks = s.flag_stride - 1;
-  if (s.k > 0) init_waits(s_wlo, s_whi, chunks);
   const int n = s.k + s.m;
   const int lo = s.n_sink, hi = n - s.recent;
   const int q = s.budget - (n - (hi - lo));      // unprotected rows to keep (>= 1)
   const float* old_score = L.score_st + (size_t)bh * s.cap;
   const float* new_score = L.new_score + (size_t)bh * s.new_stride;
   const int i0 = tid * kPer;
+  auto clampj = [&](int r) { return min(max(r - i0, 0), kPer); };
+  const uint32_t valid = bit_range(0, clampj(n));          // rows below n
+  const uint32_t cand = bit_range(clampj(lo), clampj(hi)); // unprotected rows
+  const uint32_t prot = valid & ~cand;
+  const uint32_t old = bit_range(0, clampj(s.k));          // rows kept before the call
 
+  auto score_at = [&](int i) { return i < n ? (i < s.k ? old_score[i] : new_score[i - s.k]) : 0.f; };
+  auto to_key = [&](float x) { return order_key(s.keep_low ? -x : x); };
   uint32_t key[kPer];
+  bool vec = false;
+  if constexpr (kPer % 4 == 0) {
+    // 16-byte loads when no group of 4 rows straddles k and both score planes are 16-byte aligned
+    vec = ((s.k | s.cap | s.new_stride) & 3) == 0 &&
+          ((reinterpret_cast<uintptr_t>(L.score_st) | reinterpret_cast<uintptr_t>(L.new_score)) & 15) == 0;
+  }
+  if (vec) {
+#pragma unroll
+    for (int g = 0; g < kPer / 4; ++g) {
+      const int i = i0 + 4 * g;
+      float4 v;
+      if (i + 4 <= n) {
+        v = i < s.k ? *reinterpret_cast<const float4*>(old_score + i)
+                    : *reinterpret_cast<const float4*>(new_score + (i - s.k));
+      } else {
+        v = make_float4(score_at(i), score_at(i + 1), score_at(i + 2), score_at(i + 3));
+      }
+      key[4 * g] = to_key(v.x);
+      key[4 * g + 1] = to_key(v.y);
+      key[4 * g + 2] = to_key(v.z);
+      key[4 * g + 3] = to_key(v.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) key[j] = to_key(score_at(i0 + j));
+  }
   uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
-    const int i = i0 + j;
-    float sc = 0.f;
-    if (i < n) sc = i < s.k ? old_score[i] : new_score[i - s.k];
-    key[j] = order_key(s.keep_low ? -sc : sc);
-    if (i >= lo && i < hi) {
+    if (cand & (1u << j)) {
       kmin = min(kmin, key[j]);
       kmax = max(kmax, key[j]);
     }
   }
   int* flags = L.flags + (size_t)bh * s.flag_stride;
   for (int j = tid; j < s.flag_stride; j += kThreads) flags[j] = 0;   // flags and chunk counter
+  for (int b = tid; b < kBins; b += kThreads) hist[0][b] = 0u;
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   if (lane == 0) {
-    s_min[warp] = kmin;
-    s_max[warp] = kmax;
+    s_red[0][warp] = kmin;
+    s_red[1][warp] = kmax;
   }
   if (tid == 0) {
     s_first = s.k;
     s_old_kept = 0;
   }
   __syncthreads();
-  if (warp == 0) {
-    uint32_t a = lane < kWarps ? s_min[lane] : 0xffffffffu;
-    uint32_t b = lane < kWarps ? s_max[lane] : 0u;
-    a = __reduce_min_sync(0xffffffffu, a);
-    b = __reduce_max_sync(0xffffffffu, b);
-    if (lane == 0) {
-      s_min[0] = a;
-      s_max[0] = b;
-    }
-  }
-  __syncthreads();
-  const uint32_t all_min = s_min[0], all_max = s_max[0];
+  const uint32_t all_min = __reduce_min_sync(0xffffffffu, lane < kWarps ? s_red[0][lane] : 0xffffffffu);
+  const uint32_t all_max = __reduce_max_sync(0xffffffffu, lane < kWarps ? s_red[1][lane] : 0u);
   // every unprotected key shares the top `common` bits
   const int common = all_min == all_max ? 32 : __clz(all_min ^ all_max);
   uint32_t mask = common == 0 ? 0u : (common == 32 ? 0xffffffffu : ~(0xffffffffu >> common));
-  uint32_t prefix = all_min & mask, rem = (uint32_t)q;
+  uint32_t prefix = all_min & mask, rem = (uint32_t)q, nbin = (uint32_t)(hi - lo);
   int low = 32 - common;                          // unresolved low bits
-  while (low > 0) {
+  int cur = 0;
+  while (low > 0 && rem < nbin) {
     const int w = low < kDigitBits ? low : kDigitBits;
     const int shift = low - w;
     const uint32_t dmask = (1u << w) - 1u;
-    for (int b = tid; b < kBins; b += kThreads) hist[b] = 0u;
+    uint32_t* h = hist[cur];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if ((cand & (1u << j)) && (key[j] & mask) == prefix) atomicAdd(&h[(key[j] >> shift) & dmask], 1u);
+    for (int b = tid; b < kBins; b += kThreads) hist[cur ^ 1][b] = 0u;   // the next pass's histogram
     __syncthreads();
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int i = i0 + j;
-      if (i >= lo && i < hi && (key[j] & mask) == prefix) atomicAdd(&hist[(key[j] >> shift) & dmask], 1u);
-    }
-    __syncthreads();
-    // bins from the top: thread t owns bins (nb-1-t*bpt) downwards
-    const int nb = 1 << w;
-    constexpr int kBpt = kBins / kThreads;        // bins per thread at full width
-    const int bpt = nb >= kThreads ? nb / kThreads : 1;
-    uint32_t cnt[kBpt > 0 ? kBpt : 1];
-    uint32_t sum = 0u;
-    const int top = nb - 1 - tid * bpt;
-#pragma unroll
-    for (int j = 0; j < (kBpt > 0 ? kBpt : 1); ++j) {
-      cnt[j] = (j < bpt && top - j >= 0) ? hist[top - j] : 0u;
-      sum += cnt[j];
-    }
-    uint32_t total;
-    const uint32_t above = block_excl_sum<kThreads>(sum, scan, &total);   // counts of higher bins
-    if (above < rem && rem <= above + sum) {
-      uint32_t acc = above;
-#pragma unroll
-      for (int j = 0; j < (kBpt > 0 ? kBpt : 1); ++j) {
-        if (acc + cnt[j] >= rem) {
-          s_prefix = prefix | ((uint32_t)(top - j) << shift);
-          s_rem = rem - acc;
-          break;
-        }
-        acc += cnt[j];
+    if (warp == 0) {
+      uint32_t above, count;
+      const int bin = warp_find_bin(h, rem, &above, &count);
+      if (lane == 0) {
+        s_prefix = prefix | ((uint32_t)bin << shift);
+        s_rem = rem - above;
+        s_nbin = count;
       }
     }
     __syncthreads();
     prefix = s_prefix;
     rem = s_rem;
+    nbin = s_nbin;
     mask |= dmask << shift;
     low = shift;
+    cur ^= 1;
   }
-  const uint32_t T = prefix, eq_quota = rem;
+  const uint32_t eq_quota = rem;                  // rows of the final bin admitted in index order
 
-  // ordered admission over the contiguous per-thread segments
-  uint32_t eq_count = 0u;
+  // rows kept outright (protected, or masked key above the prefix) and rows of the final bin
+  uint32_t gt = prot, eq = 0u;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
-    const int i = i0 + j;
-    eq_count += (i >= lo && i < hi && key[j] == T) ? 1u : 0u;
-  }
-  uint32_t total;
-  const uint32_t eq_before = block_excl_sum<kThreads>(eq_count, scan, &total);
-  uint32_t keep_bits = 0u, eb = eq_before;
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int i = i0 + j;
-    if (i >= n) continue;
-    const bool prot = i < lo || i >= hi;
-    bool keep = prot || key[j] > T;
-    if (!prot && key[j] == T) keep = eb++ < eq_quota;
-    if (keep) keep_bits |= 1u << j;
-  }
-  uint32_t dest = block_excl_sum<kThreads>((uint32_t)__popc(keep_bits), scan, &total);
-  int32_t* src_map = L.src_map + (size_t)bh * s.cap;
-  const int chunk_shift = __ffs(s.chunk) - 1;         // compaction chunks are 32 or 64 rows: a power of two
-  int first_drop = s.k;
-  uint32_t old_kept = 0u;
-  // wait ranges: the thread's rows and destinations both increase, so each source chunk's
-  // destination chunks form one run; it is recorded once per run
-  int run_cs = -1, run_lo = 0, run_hi = -1;
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int i = i0 + j;
-    if (i >= n) continue;
-    if (keep_bits & (1u << j)) {
-      if (dest < (uint32_t)s.budget) src_map[dest] = i;
-      else raise_device_error(P.err, kDevBadIndex);
-      if (i < s.k) {
-        ++old_kept;
-        const int cd = (int)dest >> chunk_shift, cs = i >> chunk_shift;
-        if (cd < cs) {
-          if (cs != run_cs) {
-            if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
-            run_cs = cs;
-            run_lo = cd;
-          }
-          run_hi = cd;
-        }
-      }
-      ++dest;
-    } else if (i < s.k && i < first_drop) {
-      first_drop = i;
+    if (cand & (1u << j)) {
+      const uint32_t mk = key[j] & mask;
+      if (mk > prefix) gt |= 1u << j;
+      else if (mk == prefix) eq |= 1u << j;
     }
   }
-  if (run_cs >= 0) note_wait_range(s_wlo, s_whi, run_cs, run_lo, run_hi);
-  // the first dropped kept row: one shared atomic per warp (a per-thread atomic on one address
-  // serialises hundreds of updates)
-  const int wfirst = __reduce_min_sync(0xffffffffu, first_drop);
-  if (lane == 0 && wfirst < s.k) atomicMin(&s_first, wfirst);
-  const uint32_t wsum = __reduce_add_sync(0xffffffffu, old_kept);
-  if (lane == 0 && wsum) atomicAdd(&s_old_kept, (int)wsum);
+  const uint32_t n_gt = (uint32_t)__popc(gt), n_eq = (uint32_t)__popc(eq);
+  const uint32_t packed = n_gt | (n_eq << 16);
+  const uint32_t pincl = warp_incl_sum(packed);
+  if (lane == 31) s_cnt[warp] = pincl;
+  __syncthreads();
+  const uint32_t wtot = lane < kWarps ? s_cnt[lane] : 0u;
+  const uint32_t wbefore = __shfl_sync(0xffffffffu, warp_incl_sum(wtot) - wtot, warp);
+  const uint32_t before = wbefore + pincl - packed;
+  const uint32_t eq_before = before >> 16;
+  const uint32_t dest = (before & 0xffffu) + min(eq_quota, eq_before);
+  // the first r rows of the final bin are admitted
+  const uint32_t r = eq_quota > eq_before ? min(n_eq, eq_quota - eq_before) : 0u;
+  uint32_t eq_keep = eq;
+  if (r < n_eq) {
+    uint32_t rest = eq;
+    for (uint32_t t = 0; t < r; ++t) rest &= rest - 1u;
+    eq_keep = eq & ~rest;
+  }
+  const uint32_t keep = gt | eq_keep;
+
+  int32_t* src_map = L.src_map + (size_t)bh * s.cap;
+  {
+    uint32_t kb = keep;
+    uint32_t d = dest;
+    while (kb) {
+      const int j = __ffs(kb) - 1;
+      kb &= kb - 1u;
+      if (d < (uint32_t)s.budget) src_map[d] = i0 + j;
+      else raise_device_error(P.err, kDevBadIndex);
+      ++d;
+    }
+  }
+  // kept rows below k. Survivors keep their order, so the kept rows of source chunk c take the
+  // destinations [kb(c), kb(c + 1)), kb(c) being the survivors before the chunk's first row (and
+  // kb at k the kept rows that survive); the thread holding a chunk's first row records kb(c).
+  const int chunk_shift = __ffs(s.chunk) - 1;     // compaction chunks are a power of two
+  for (int c0 = ((i0 + s.chunk - 1) >> chunk_shift) << chunk_shift; c0 < min(i0 + kPer, s.k); c0 += s.chunk)
+    s_kb[c0 >> chunk_shift] = (int)(dest + (uint32_t)__popc(keep & bit_range(0, c0 - i0)));
+  const uint32_t old_keep = keep & old;
+  const uint32_t drop = old & ~keep;
+  // the first dropped kept row and the survivor count: one shared atomic per warp
+  const int wfirst = __reduce_min_sync(0xffffffffu, drop ? i0 + __ffs(drop) - 1 : s.k);
+  const uint32_t wkept = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(old_keep));
+  if (lane == 0) {
+    if (wfirst < s.k) atomicMin(&s_first, wfirst);
+    if (wkept) atomicAdd(&s_old_kept, (int)wkept);
+  }
   __syncthreads();
   if (tid == 0) L.meta[bh] = make_int2(s_first, s_old_kept);
-  if (s.k > 0) store_waits(s_wlo, s_whi, L.waits + (size_t)bh * chunks, chunks);
+  if (s.k > 0) {
+    // wait ranges of the compaction: the kept rows of source chunk c are read by the destination
+    // chunks [kb(c) / C, (kb(c + 1) - 1) / C]; those below c must read them before chunk c is
+    // overwritten (empty: hi < lo)
+    int2* out = L.waits + (size_t)bh * chunks;
+    const int old_chunks = (s.k + s.chunk - 1) >> chunk_shift;
+    for (int c = tid; c < chunks; c += kThreads) {
+      int2 wr = make_int2(0x7fffffff, -1);
+      if (c < old_chunks) {
+        const int a = s_kb[c], b = c + 1 < old_chunks ? s_kb[c + 1] : s_old_kept;
+        if (b > a) {
+          const int lo_c = a >> chunk_shift, hi_c = min((b - 1) >> chunk_shift, c - 1);
+          if (lo_c <= hi_c) wr = make_int2(lo_c, hi_c);
+        }
+      }
+      out[c] = wr;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
