@@ -62,9 +62,10 @@ __device__ __forceinline__ uint32_t block_excl_sum(uint32_t x, uint32_t* scratch
 // whose masked key is above the prefix are kept, and of the rows whose masked
 // key equals it, the first eq_quota in index order. One block scan of the
 // per-thread counts of both classes gives each thread its first destination;
-// each thread then writes the source row of each of its survivors to
-// src_map[destination]. Also zeroes the unit's compaction flags and chunk
-// counter.
+// each thread then writes the source row of each of its survivors to a
+// shared copy of src_map (budget words of dynamic shared memory), which the
+// block stores coalesced at the end. Also zeroes the unit's compaction flags
+// and chunk counter.
 // ---------------------------------------------------------------------------
 constexpr int kDigitBits = 11;
 constexpr int kBins = 1 << kDigitBits;
@@ -153,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __gr
   __shared__ uint32_t s_prefix, s_rem, s_nbin;
   __shared__ int s_first, s_old_kept;
   __shared__ int s_kb[kMaxWaitChunks];            // per source chunk holding kept rows: survivors before it
+  extern __shared__ int32_t s_map[];              // [budget] source row of each destination
   const Shape& s = P.s;
   const int bhn = s.batch * s.heads;
   const int u = blockIdx.x;
@@ -290,14 +292,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __gr
   }
   const uint32_t keep = gt | eq_keep;
 
-  int32_t* src_map = L.src_map + (size_t)bh * s.cap;
   {
     uint32_t kb = keep;
     uint32_t d = dest;
     while (kb) {
       const int j = __ffs(kb) - 1;
       kb &= kb - 1u;
-      if (d < (uint32_t)s.budget) src_map[d] = i0 + j;
+      if (d < (uint32_t)s.budget) s_map[d] = i0 + j;
       else raise_device_error(P.err, kDevBadIndex);
       ++d;
     }
@@ -318,6 +319,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) select_kernel(const __gr
     if (wkept) atomicAdd(&s_old_kept, (int)wkept);
   }
   __syncthreads();
+  int32_t* src_map = L.src_map + (size_t)bh * s.cap;
+  for (int d = tid; d < s.budget; d += kThreads) src_map[d] = s_map[d];
   if (tid == 0) L.meta[bh] = make_int2(s_first, s_old_kept);
   if (s.k > 0) {
     // wait ranges of the compaction: the kept rows of source chunk c are read by the destination
@@ -506,19 +509,35 @@ cudaError_t launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream
 
 }  // namespace
 
+// The register variants take budget words of dynamic shared memory (budget < n <= kThreads * kPer).
+template <int kThreads, int kPer, int kMinBlocks>
+cudaError_t allow_map(cudaError_t e) {
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(select_kernel<kThreads, kPer, kMinBlocks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)(kThreads * kPer * sizeof(int32_t)));
+}
+
 cudaError_t prepare_select() {
-  // The shared-memory variant serves the largest row counts. The attribute is
-  // always the compiled maximum: it is per function and device, so a smaller
+  // The shared-memory variant serves the largest row counts. The attributes are
+  // always the compiled maxima: they are per function and device, so a smaller
   // value set for one cache would break launches of a larger one.
   const int bytes = (int)(EVICT_MAX_SELECT_ROWS * sizeof(uint32_t));
-  return cudaFuncSetAttribute(select_smem_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaFuncSetAttribute(select_smem_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  e = allow_map<256, 4, 1>(e);
+  e = allow_map<256, 8, 1>(e);
+  e = allow_map<512, 16, 2>(e);
+  e = allow_map<1024, 8, 1>(e);
+  e = allow_map<1024, 12, 1>(e);
+  e = allow_map<1024, 17, 1>(e);
+  return allow_map<1024, 24, 1>(e);
 }
 
 cudaError_t launch_select(const GroupParams& P, cudaStream_t st) {
   const int n = P.s.k + P.s.m;
   const dim3 grid(P.s.n_layers * P.s.batch * P.s.heads);
-  if (n <= 256 * 4) return launch(select_kernel<256, 4>, grid, dim3(256), 0, st, P);
-  if (n <= 256 * 8) return launch(select_kernel<256, 8>, grid, dim3(256), 0, st, P);
+  const size_t map = (size_t)P.s.budget * sizeof(int32_t);   // register variants: the shared src_map
+  if (n <= 256 * 4) return launch(select_kernel<256, 4>, grid, dim3(256), map, st, P);
+  if (n <= 256 * 8) return launch(select_kernel<256, 8>, grid, dim3(256), map, st, P);
   if (n <= 512 * 16) {
     // more (b, h) units than SMs: 512-thread CTAs, two per SM, keep every unit in one wave
     int dev = 0, sms = 0;
@@ -526,13 +545,13 @@ cudaError_t launch_select(const GroupParams& P, cudaStream_t st) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     if ((int)grid.x > sms && (int)grid.x <= 2 * sms)
-      return launch(select_kernel<512, 16, 2>, grid, dim3(512), 0, st, P);
+      return launch(select_kernel<512, 16, 2>, grid, dim3(512), map, st, P);
   }
-  if (n <= 1024 * 8) return launch(select_kernel<1024, 8>, grid, dim3(1024), 0, st, P);
+  if (n <= 1024 * 8) return launch(select_kernel<1024, 8>, grid, dim3(1024), map, st, P);
   // the fewest keys per thread that hold n: less serial work per pass, no register spills
-  if (n <= 1024 * 12) return launch(select_kernel<1024, 12>, grid, dim3(1024), 0, st, P);
-  if (n <= 1024 * 17) return launch(select_kernel<1024, 17>, grid, dim3(1024), 0, st, P);
-  if (n <= 1024 * 24) return launch(select_kernel<1024, 24>, grid, dim3(1024), 0, st, P);
+  if (n <= 1024 * 12) return launch(select_kernel<1024, 12>, grid, dim3(1024), map, st, P);
+  if (n <= 1024 * 17) return launch(select_kernel<1024, 17>, grid, dim3(1024), map, st, P);
+  if (n <= 1024 * 24) return launch(select_kernel<1024, 24>, grid, dim3(1024), map, st, P);
   return launch(select_smem_kernel<1024>, grid, dim3(1024), (size_t)n * sizeof(uint32_t), st, P);
 }
 
