@@ -74,31 +74,6 @@ def test_knorm_single_sequence_one_block_and_token_by_token():
         assert np.array_equal(to_bits(one[2])[0, 0], keep_plain)
 
 
-@pytest.mark.parametrize("method", ["knorm", "qfilters"])
-@pytest.mark.parametrize("B,H,S,budget", [(1, 3, 9000, 3000), (1, 3, 14000, 700), (1, 3, 30000, 5000),
-                                          (1, 3, 70000, 4000), (8, 6, 10000, 2000)])
-def test_ties_in_large_selections(method, B, H, S, budget):
-    # more than 4096 rows per unit: the register selection with 8 to 24 keys per thread and, past
-    # 24576 rows, the shared-memory one; tie pools, NaN, +-0 and +-inf rows lie on both sides of
-    # thread-segment boundaries, and a second block makes the kept rows move
-    g = synth.rng(78 + S)
-    pool = synth.f32_to_bf16_bits(g.standard_normal((7, 128)).astype(np.float32))
-    k = pool[g.integers(0, 7, size=(B, H, S))]
-    for r in (4095, 4096, 4097, 8191, 8192, S - 3):
-        k[0, 0, r] = 0                                # zero keys at CTA boundaries
-    k[0, 1, 4096, 5] = 0x7FC0                         # NaN
-    k[0, 1, 4095, 5] = 0x7F80                         # +inf entry
-    k[0, 2, 8192, 9] = 0xFF80                         # -inf entry
-    k[0, 2, 100:140, :] = 0x8000                      # -0 keys
-    v = synth.f32_to_bf16_bits(g.standard_normal((B, H, S, 128)).astype(np.float32))
-    kw = dict(n_sink=5, recent=7)
-    if method == "qfilters":
-        kw.update(filters=synth.unit_vectors(synth.rng(6), H).astype(np.float32), sign=-1)
-    cut = S // 2
-    gpu, ref = _pair(method, B, H, budget, max_block=S - cut, **kw)
-    _feed(gpu, ref, k, v, [0, cut, S], check_each=True, what=f"large-selection ties S={S}")
-
-
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("method,extra", [("knorm", {"keep_low": True}), ("knorm", {"keep_low": False}),
                                           ("qfilters", {"sign": 1}), ("qfilters", {"sign": -1})])
@@ -164,6 +139,30 @@ def test_ties_in_large_selections(method, B, H, S, budget):
     cut = S // 2
     gpu, ref = _pair(method, B, H, budget, max_block=S - cut, **kw)
     _feed(gpu, ref, k, v, [0, cut, S], check_each=True, what=f"large-selection ties S={S}")
+
+
+@pytest.mark.parametrize("method,extra", [("knorm", {"keep_low": True}), ("knorm", {"keep_low": False}),
+                                          ("qfilters", {"sign": 1}), ("qfilters", {"sign": -1})])
+def test_large_selections_odd_sizes_and_equal_units(method, extra):
+    # register selections of 8000 and 9002 rows with an odd budget, storage and kept count (scalar
+    # score loads; compaction chunks that start inside a thread's rows): continuous scores end
+    # the radix passes once the whole bin is admitted (two-signed projections take up to three
+    # passes); head 1 holds one key repeated (every candidate equal: no pass at all); NaN and
+    # +-inf rows sit at thread boundaries
+    B, H, S, budget = 2, 3, 14001, 3001
+    g = synth.rng(4242)
+    k = synth.f32_to_bf16_bits((g.standard_normal((B, H, S, 128)) * 1.5).astype(np.float32))
+    k[:, 1] = k[0, 1, 17]                             # every row of head 1 equal
+    k[0, 0, 2999, 3] = 0x7FC0                         # NaN in the first kept block's last row
+    k[0, 2, 8191, 7] = 0x7F80                         # +inf entry
+    k[1, 2, 8192, 7] = 0xFF80                         # -inf entry
+    k[1, 0, 4000:4016, :] = 0x8000                    # -0 keys
+    v = synth.f32_to_bf16_bits(g.standard_normal((B, H, S, 128)).astype(np.float32))
+    kw = dict(n_sink=3, recent=5, **extra)
+    if method == "qfilters":
+        kw["filters"] = synth.unit_vectors(synth.rng(8), H).astype(np.float32)
+    gpu, ref = _pair(method, B, H, budget, max_block=6001, **kw)
+    _feed(gpu, ref, k, v, [0, 2999, 8000, 14001], check_each=True, what=f"odd sizes {method} {extra}")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
