@@ -1165,8 +1165,15 @@ __device__ __forceinline__ float hash_unit(int i, int j) {
 //   p_0 = 1, p_1 = d_0 - x, p_{i+1} = (d_i - x) p_i - e_{i-1}^2 p_{i-1}.
 // This is the pivot recurrence q_i = p_i / p_{i-1} without its division
 // (the same rounding behaviour up to scaling); a minor smaller than 2^-24 of
-// its predecessor counts as a negative pivot, and every second step both
-// minors are rescaled by an exact power of two when they leave [2^-48, 2^48].
+// its predecessor counts as a negative pivot, and every fourth step both
+// minors are scaled by the exact power of two that brings the larger into
+// [1, 2). T is similar to a unit-trace positive semi-definite matrix, so
+// |d|, |e| <= 1 and |x| <= 1.01 tnorm <= 3.03: a step multiplies the larger
+// minor by at most 5.03, the guard keeps each minor at least 2^-24 of its
+// predecessor, and a minor is at most 4.03 + 2^24 times its predecessor. So
+// after a scaling both minors are at least about 2^-24, and four steps later
+// every minor lies in [2^-121, 2^11]: none becomes subnormal or overflows,
+// and exact power-of-two scaling changes no count.
 __device__ __forceinline__ void sturm_count2(const float2* de2, const float (&x)[2], int (&cnt)[2]) {
   constexpr float kTiny = 5.9604645e-08f;          // 2^-24
   float u[2], v[2];
@@ -1179,7 +1186,7 @@ __device__ __forceinline__ void sturm_count2(const float2* de2, const float (&x)
     cnt[k] = v[k] < 0.f ? 1 : 0;
   }
   float2 tn = de2[1];
-#pragma unroll 2
+#pragma unroll 4
   for (int i = 1; i < kHeadDim; ++i) {
     const float2 t = tn;
     if (i + 1 < kHeadDim) tn = de2[i + 1];
@@ -1192,11 +1199,11 @@ __device__ __forceinline__ void sturm_count2(const float2* de2, const float (&x)
       u[k] = v[k];
       v[k] = w;
     }
-    if (i & 1) {
+    if ((i & 3) == 3) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int ex = (int)((__float_as_uint(fmaxf(fabsf(u[k]), fabsf(v[k]))) >> 23) & 0xff) - 127;
-        const float sc = (ex > 48 || ex < -48) ? __uint_as_float((uint32_t)(127 - ex) << 23) : 1.f;
+        const float sc = __uint_as_float((uint32_t)(127 - ex) << 23);
         u[k] *= sc;
         v[k] *= sc;
       }
@@ -1643,30 +1650,49 @@ __global__ void __launch_bounds__(kEigThreads, kR <= 16 ? 2 : 1)
       }
     }
     __syncthreads();
-    if (warp == 0) {                                    // right-looking Cholesky in place, lane = row
-      for (int k = 0; k < r; ++k) {
-        const float dk = s.gram[k][k];
-        const float dinv = dk > 1e-20f ? rsqrtf(dk) : 0.f;
-        if (lane >= k && lane < r) s.gram[lane][k] *= dinv;   // L[k][k] = sqrt(dk)
-        if (lane == 0) s.lam[k] = dinv;                        // reciprocal pivots
-        __syncwarp();
-        if (lane > k && lane < r) {
-          const float lik = s.gram[lane][k];
-#pragma unroll 4
-          for (int m = k + 1; m <= lane; ++m) s.gram[lane][m] = fmaf(-lik, s.gram[m][k], s.gram[lane][m]);
+    if (warp == 0) {
+      // right-looking Cholesky, lane = row: the row lives in registers and column k of L comes
+      // from its rows' lanes by shuffles (the same multiply-adds in the same order as a
+      // shared-memory update, without a shared-memory round trip per element)
+      float g[kR];
+#pragma unroll
+      for (int m = 0; m < kR; ++m) g[m] = (lane < r && m < r) ? s.gram[lane][m] : 0.f;
+#pragma unroll
+      for (int k = 0; k < kR; ++k) {
+        if (k < r) {
+          const float dk = __shfl_sync(0xffffffffu, g[k], k);
+          const float dinv = dk > 1e-20f ? rsqrtf(dk) : 0.f;
+          if (lane >= k) g[k] *= dinv;                  // L[k][k] = sqrt(dk)
+          if (lane == 0) s.lam[k] = dinv;               // reciprocal pivots
+          const float lik = g[k];
+#pragma unroll
+          for (int m = k + 1; m < kR; ++m) {
+            const float lmk = __shfl_sync(0xffffffffu, g[k], m);
+            if (lane > k && m <= lane) g[m] = fmaf(-lik, lmk, g[m]);
+          }
         }
-        __syncwarp();
       }
+#pragma unroll
+      for (int m = 0; m < kR; ++m)
+        if (lane < r && m < r) s.gram[lane][m] = g[m];
     }
     __syncthreads();
-    if (tid < n) {                                      // forward substitution in place, one column per thread
-#pragma unroll 1
-      for (int ia = 0; ia < r; ++ia) {
-        float acc = s.z[ia][tid];
-#pragma unroll 4
-        for (int ib = 0; ib < ia; ++ib) acc = fmaf(-s.gram[ia][ib], s.z[ib][tid], acc);
-        s.z[ia][tid] = acc * s.lam[ia];
+    if (tid < n) {                                      // forward substitution, one column per thread, in registers
+      float zc[kR];
+#pragma unroll
+      for (int ia = 0; ia < kR; ++ia) zc[ia] = ia < r ? s.z[ia][tid] : 0.f;
+#pragma unroll
+      for (int ia = 0; ia < kR; ++ia) {
+        if (ia < r) {
+          float acc = zc[ia];
+#pragma unroll
+          for (int ib = 0; ib < ia; ++ib) acc = fmaf(-s.gram[ia][ib], zc[ib], acc);
+          zc[ia] = acc * s.lam[ia];
+        }
       }
+#pragma unroll
+      for (int ia = 0; ia < kR; ++ia)
+        if (ia < r) s.z[ia][tid] = zc[ia];
     }
     __syncthreads();
   }
@@ -1689,16 +1715,18 @@ __global__ void __launch_bounds__(kEigThreads, kR <= 16 ? 2 : 1)
       for (int blk = kBtBlocks - 1; blk >= 0; --blk) {
         const int j0 = blk * kBtBlock;
         const int nb = min(kBtBlock, kEigSteps - j0);
+        // the block's reflection vectors stay in registers for both the dots and the update
         float sdot[kBtBlock];
+        float4 hvr[kBtBlock][4];
 #pragma unroll
         for (int k = 0; k < kBtBlock; ++k) {
           float acc = 0.f;
-          if (k < nb) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float4 v = hv_chunk(s.hv, j0 + k, q + 8 * i);
+          for (int i = 0; i < 4; ++i) {
+            const float4 v = k < nb ? hv_chunk(s.hv, j0 + k, q + 8 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            hvr[k][i] = v;
+            if (k < nb)
               acc = fmaf(v.x, y[4 * i], fmaf(v.y, y[4 * i + 1], fmaf(v.z, y[4 * i + 2], fmaf(v.w, y[4 * i + 3], acc))));
-            }
           }
           sdot[k] = acc;
         }
@@ -1719,7 +1747,7 @@ __global__ void __launch_bounds__(kEigThreads, kR <= 16 ? 2 : 1)
           if (k < nb) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float4 v = hv_chunk(s.hv, j0 + k, q + 8 * i);
+              const float4 v = hvr[k][i];
               y[4 * i] = fmaf(-coef[k], v.x, y[4 * i]);
               y[4 * i + 1] = fmaf(-coef[k], v.y, y[4 * i + 1]);
               y[4 * i + 2] = fmaf(-coef[k], v.z, y[4 * i + 2]);
