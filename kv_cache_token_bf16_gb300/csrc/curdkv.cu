@@ -1317,8 +1317,9 @@ __global__ void __launch_bounds__(kEigThreads, kR <= 16 ? 2 : 1)
     }
     const float nu = s.vs[bp][j];
     const float omega = fmaf(-Kp, nu, beta_prev * s.pp[bp][j]);
-    // v_{j-1}, w_{j-1}, x_j of rows 4 lane .. +3 (warp-private), |x_j|^2
+    // v_{j-1}, w_{j-1}, x_j of rows 4 lane .. +3 (warp-private), |x_j|^2; x_j stays in xq
     float ss = 0.f;
+    float xq[4];
     {
       const int q0 = 4 * lane;
       const float4 c4 = *reinterpret_cast<const float4*>(&s.cb[bp][q0]);
@@ -1326,7 +1327,7 @@ __global__ void __launch_bounds__(kEigThreads, kR <= 16 ? 2 : 1)
       const float4 p4 = *reinterpret_cast<const float4*>(&s.pp[bp][q0]);
       const float cq[4] = {c4.x, c4.y, c4.z, c4.w}, vq[4] = {v4.x, v4.y, v4.z, v4.w};
       const float pq[4] = {p4.x, p4.y, p4.z, p4.w};
-      float wq[4], xq[4];
+      float wq[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int q = q0 + k;
@@ -1345,13 +1346,13 @@ __global__ void __launch_bounds__(kEigThreads, kR <= 16 ? 2 : 1)
     for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float x0 = wv[2 * n + j + 1];
     const float tail = ss - x0 * x0;
-    float beta = 0.f, alpha = x0, delta = 0.f;
-    if (tail > 0.f && ss > kEigTinyColumn) {
-      const float sigma = ss * rsqrtf(ss);
-      alpha = x0 >= 0.f ? -sigma : sigma;
-      delta = -alpha;                                   // v[j+1] = x0 - alpha
-      beta = __fdividef(1.f, sigma * (sigma + fabsf(x0)));
-    }
+    // branch-free (selects), so that this chain and the update below share one basic block
+    const bool reflect = tail > 0.f && ss > kEigTinyColumn;
+    const float ssr = reflect ? ss : 1.f;
+    const float sigma = ssr * rsqrtf(ssr);
+    const float alpha = reflect ? (x0 >= 0.f ? -sigma : sigma) : x0;
+    const float delta = reflect ? -alpha : 0.f;         // v[j+1] = x0 - alpha
+    const float beta = reflect ? __fdividef(1.f, sigma * (sigma + fabsf(x0))) : 0.f;
     // this thread's rows: v_{j-1}, w_{j-1}, x_j
     float pvr[8], pwr[8], xr[8];
     {
@@ -1439,12 +1440,11 @@ __global__ void __launch_bounds__(kEigThreads, kR <= 16 ? 2 : 1)
     }
     if (warp == 0) {                                    // v_j for the next step and the back-transform
       const int q0 = 4 * lane;
-      const float4 x4 = *reinterpret_cast<const float4*>(wv + 2 * n + q0);
       float4 v4;
-      v4.x = x4.x + (q0 == j1 ? delta : 0.f);
-      v4.y = x4.y + (q0 + 1 == j1 ? delta : 0.f);
-      v4.z = x4.z + (q0 + 2 == j1 ? delta : 0.f);
-      v4.w = x4.w + (q0 + 3 == j1 ? delta : 0.f);
+      v4.x = xq[0] + (q0 == j1 ? delta : 0.f);
+      v4.y = xq[1] + (q0 + 1 == j1 ? delta : 0.f);
+      v4.z = xq[2] + (q0 + 2 == j1 ? delta : 0.f);
+      v4.w = xq[3] + (q0 + 3 == j1 ? delta : 0.f);
       *reinterpret_cast<float4*>(&s.vs[b][q0]) = v4;
       if (lane >= hv_first_chunk(j))                    // the chunks before are exactly zero
         *reinterpret_cast<float4*>(&s.hv[hv_row_base(j) + 4 * (lane - hv_first_chunk(j))]) = v4;
